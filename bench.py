@@ -1,0 +1,519 @@
+#!/usr/bin/env python3
+"""Benchmark of the single-GPU MoE layer with Dual-Batch Overlap.
+
+One step = one pass of the whole layer -- route, plan, dispatch, expert FFN and
+combine on two ubatches overlapped on a compute and a comm stream
+(moe_layer_dbo) -- over one batch of synthetic input, replayed as a CUDA graph.
+Default workload: the Qwen3-30B-A3B shaped decode layer (T=256 split 128/128,
+hidden 2048, 128 experts top-8, intermediate 768, bf16, uniform routing).
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload on its own GPU (the layer has no cross-GPU step), so the
+scaling is weak and the value is the tokens of all ranks over the slowest rank's
+time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from moe_expert_dispatch_route_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (route->dispatch->GEMM->combine, DBO) at 1 GB300; % roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+COMM_SMS = 16
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_decode", choices=sorted(W.ALL))
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--routing", default=None, choices=[None, "uniform", "zipf"])
+    ap.add_argument("--comm-sms", type=int, default=COMM_SMS)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the DBO-gain and e2e legs")
+    return ap.parse_args()
+
+
+def workload(args):
+    wl = W.ALL[args.workload]
+    if args.T:
+        wl = wl.with_(T=args.T)
+    if args.routing:
+        wl = wl.with_(routing=args.routing)
+    return wl
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            self.sel = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                   "-f", self.path]
+            if self.sel:
+                cmd[1:1] = ["-i", self.sel]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if not self.proc:
+            return out
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        try:
+            with open(self.path) as f:
+                rows = [ln.strip().split(",") for ln in f if ln.strip()]
+            os.unlink(self.path)
+        except Exception:
+            return out
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if sm:
+            out.update(sm_mhz=statistics.median(sm), sm_max_mhz=max(mx), reasons=sorted(reasons),
+                       samples=len(sm))
+        return out
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def launches_per_step(wl, split_two: bool) -> int:
+    """Kernels this library launches for one layer call (route, plan passes, dispatch,
+    the two FFN kernels, combine -- per ubatch)."""
+    kk = wl.top_k + wl.num_shared
+    tpc = max(1, 4096 // kk)
+    sizes = [wl.split, wl.T - wl.split] if split_two else [wl.T]
+    n = 0
+    for Tu in sizes:
+        chunks = max(1, math.ceil(Tu / tpc))
+        n += 1 + (2 if chunks > 1 else 1) + 1 + 2 + 1
+    return n
+
+
+def ffn_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_expert_dispatch_route_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("ffn") or name in ("common.cuh", "kernels.h", "tc_ptx.cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag: str, wl_name: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/, only if the
+    FFN sources are unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", f"{kernel_tag}_{wl_name}.txt")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for ln in f:
+            if ":" in ln:
+                k, v = ln.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("ffn_source_hash") != ffn_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    from moe_expert_dispatch_route_gb300 import binding as B
+    from moe_expert_dispatch_route_gb300 import synth
+
+    wl = workload(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = B.config_of(wl)
+    T, H, E, k = wl.T, wl.hidden, wl.num_experts, wl.top_k
+    io = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    inp = synth.workload_inputs(wl, dev)
+    Wd = {kk_: v for kk_, v in inp.items() if kk_.startswith("w")}
+    logits, x = inp["logits"], inp["x"]
+    y = torch.zeros(T, H, dtype=io, device=dev)
+    ids = torch.zeros(T, k, dtype=torch.int32, device=dev)
+    w = torch.zeros(T, k, dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    cap, align = wl.capacity, wl.align
+    ws = torch.empty(B.moe_layer_workspace_size(cfg, T, cap, align), dtype=torch.uint8, device=dev)
+    args_c = B.layer_args(logits, x, Wd, y, ids, w, ws, None, err)
+    handle = B.moe_dbo_create()
+    comm = torch.cuda.Stream(device=dev)
+    compute = torch.cuda.Stream(device=dev)
+    comm_sms = args.comm_sms
+
+    def enqueue(split=0, same=False, a=args_c, cs=None):
+        cs = cs or torch.cuda.current_stream()
+        B.moe_layer_dbo(handle, cfg, a, T, split, 4, cap, align, comm_sms, cs, cs if same else comm)
+
+    def capture(**kw):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(compute):
+            enqueue(**kw)  # eager warm call (also builds any per-device state)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=compute):
+                enqueue(**kw, cs=compute)
+        torch.cuda.synchronize()
+        return g
+
+    def time_graph(g, steps, warmup, sample_clocks=False):
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        sampler = ClockSampler(local) if sample_clocks else None
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(compute):
+            e0.record(compute)
+            for _ in range(steps):
+                g.replay()
+            e1.record(compute)
+        torch.cuda.synchronize()
+        barrier(world)
+        clocks = sampler.stop() if sampler else None
+        return e0.elapsed_time(e1) / steps, clocks
+
+    g_dbo = capture(split=0)
+    ms, clocks = time_graph(g_dbo, args.steps, args.warmup, sample_clocks=True)
+    ms = max_over_ranks(ms, world)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error flag {int(err.item())}"
+
+    res = {}
+    two = T >= 4 and 0 < wl.split < T
+    if not args.no_extras:
+        # DBO gain: the same two ubatches serialised on one stream, and the unsplit layer
+        g_serial = capture(split=0, same=True)
+        ms_serial, _ = time_graph(g_serial, args.steps, args.warmup)
+        g_unsplit = capture(split=T)
+        ms_unsplit, _ = time_graph(g_unsplit, args.steps, args.warmup)
+        res["dbo"] = {"ms_dbo": round(ms, 5), "ms_two_ubatches_one_stream": round(ms_serial, 5),
+                      "ms_unsplit_one_stream": round(ms_unsplit, 5),
+                      "gain_vs_two_ubatches_one_stream": round(ms_serial / ms, 4),
+                      "gain_vs_unsplit": round(ms_unsplit / ms, 4), "comm_sms": comm_sms}
+        del g_serial, g_unsplit
+
+    # ---- roofline of the dominant kernel: moe_expert_ffn on ubatch 0, timed alone
+    roof = ffn_roofline(B, wl, cfg, inp, dev, args, comm_sms, compute)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_extras:
+        e2e = run_e2e(B, wl, cfg, inp, args_c, handle, comm, compute, enqueue, logits, x, y, args, world)
+
+    value = T * world / (ms / 1e3)
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "fp8e4m3"}[wl.dtype],
+        "data": "synthetic (seeded N(0,1) logits / hidden states, N(0,0.02) weights)",
+        "config": {"workload": wl.describe(), "T": T, "hidden": H, "inter": wl.inter, "experts": E,
+                   "shared": wl.num_shared, "top_k": k, "ubatches": 2 if two else 1, "split": wl.split,
+                   "layout": f"capacity {cap}" if cap else f"exact, align {align}", "comm_sms": comm_sms,
+                   "graph": "CUDA graph replay", "l2": "inputs larger than L2 (expert weights "
+                   f"{weights_bytes(wl) / 1e9:.2f} GB > 129 MB L2)", "parallelism": f"replicas x{world}"},
+        "gpu_launches": launches_per_step(wl, two) * args.steps,
+        "clocks": clocks,
+        "roofline": roof,
+        "e2e": e2e,
+    }
+    out.update(res)
+    B.moe_dbo_destroy(handle)
+    return out, wl
+
+
+def weights_bytes(wl) -> float:
+    NE = wl.num_experts + wl.num_shared
+    elt = {"f32": 4, "bf16": 2, "fp8": 1}[wl.dtype]
+    return NE * 3 * wl.hidden * wl.inter * elt
+
+
+def ffn_roofline(B, wl, cfg, inp, dev, args, comm_sms, compute):
+    pk, src = peaks()
+    T0 = wl.split if (wl.T >= 4 and 0 < wl.split < wl.T) else wl.T
+    H, I, E, S, k = wl.hidden, wl.inter, wl.num_experts, wl.num_shared, wl.top_k
+    NE, kk = E + S, k + S
+    fp8 = wl.dtype == "fp8"
+    elt = {"f32": 4, "bf16": 2, "fp8": 1}[wl.dtype]
+    io = 4 if wl.dtype == "f32" else 2
+    rows = B.moe_plan_rows(cfg, T0, wl.capacity, wl.align)
+    ids = torch.zeros(T0, k, dtype=torch.int32, device=dev)
+    w = torch.zeros(T0, k, dtype=torch.float32, device=dev)
+    counts = torch.zeros(NE, dtype=torch.int32, device=dev)
+    offsets = torch.zeros(NE + 1, dtype=torch.int32, device=dev)
+    slot_of = torch.zeros(T0, kk, dtype=torch.int32, device=dev)
+    token_of = torch.zeros(rows, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pws = torch.empty(max(B.moe_plan_workspace_size(cfg, T0), 4), dtype=torch.uint8, device=dev)
+    xe = torch.zeros(rows, H * elt, dtype=torch.uint8, device=dev)
+    xs = torch.zeros(rows, H // 128, dtype=torch.float32, device=dev) if fp8 else None
+    ye = torch.zeros(rows, H * io, dtype=torch.uint8, device=dev)
+    fws = torch.empty(B.moe_ffn_workspace_size(cfg, rows), dtype=torch.uint8, device=dev)
+    w13 = inp.get("w13", inp.get("w13_q"))
+    w2 = inp.get("w2", inp.get("w2_q"))
+    with torch.cuda.stream(compute):
+        B.moe_route(cfg, T0, inp["logits"], None, ids, w, 0, compute)
+        B.moe_plan(cfg, T0, ids, wl.capacity, wl.align, counts, offsets, slot_of, token_of, err, pws,
+                   pws.numel(), 0, compute)
+        B.moe_dispatch(cfg, T0, inp["x"], slot_of, xe, xs, 0, compute)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ffn_ctas = max(1, sms - comm_sms)
+
+    def call():
+        B.moe_expert_ffn(cfg, counts, offsets, rows, xe, xs, w13, inp.get("w13_s"), w2, inp.get("w2_s"), ye,
+                         fws, fws.numel(), err, ffn_ctas, compute)
+
+    with torch.cuda.stream(compute):
+        for _ in range(max(3, args.warmup)):
+            call()
+    torch.cuda.synchronize()
+    n = max(10, args.steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(compute):
+        e0.record(compute)
+        for _ in range(n):
+            call()
+        e1.record(compute)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / n / 1e3
+    c = counts.cpu().numpy().astype(np.int64)
+    touched = int((c > 0).sum())
+    used = int(c.sum())
+    wbytes_e = 3 * H * I * elt + (((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4 if fp8 else 0)
+    act_bytes = used * (H * elt + 2 * I * elt + H * io) + (used * (H // 128 + 2 * (I // 128)) * 4 if fp8 else 0)
+    bytes_alg = touched * wbytes_e + act_bytes
+    flops_alg = 2.0 * used * 3 * H * I
+    bw = pk["hbm_gbs"] * 1e9
+    tf = pk["bf16_tflops"] * 1e12 * (2.0 if fp8 else 1.0)   # fp8 peak = bf16 measured x nominal 2x
+    bound = "tensor" if flops_alg / tf > bytes_alg / bw else "hbm"
+    if bound == "hbm":
+        achieved, peak, unit = bytes_alg / t / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = flops_alg / t / 1e12, tf / 1e12, "TFLOP/s"
+    traffic = profiled_traffic("ffn", wl.name)
+    return {"kernel": "moe_expert_ffn (gate/up + SwiGLU, down) on ubatch 0", "bound": bound,
+            "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": unit,
+            "frac": round(achieved / peak, 4), "peak_source": f"{src} ({'fp8 = 2x bf16 nominal ratio' if fp8 and bound == 'tensor' else 'burst'})",
+            "traffic": traffic, "algorithmic_bytes": int(bytes_alg), "algorithmic_flops": flops_alg,
+            "us_per_launch": round(t * 1e6, 3), "rows": used, "experts_touched": touched,
+            "ctas": ffn_ctas}
+
+
+def run_e2e(B, wl, cfg, inp, args_c, handle, comm, compute, enqueue, logits, x, y, args, world):
+    """Same metric with host buffers: every step copies logits and x from pinned host
+    memory, runs the layer through the C ABI and copies y back."""
+    h_logits = logits.cpu().pin_memory()
+    h_x = x.cpu().pin_memory()
+    h_y = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+
+    def step():
+        with torch.cuda.stream(compute):
+            logits.copy_(h_logits, non_blocking=True)
+            x.copy_(h_x, non_blocking=True)
+            enqueue(cs=compute)
+            h_y.copy_(y, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(compute)
+    for _ in range(args.steps):
+        step()
+    e1.record(compute)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    bi = h_logits.numel() * h_logits.element_size() + h_x.numel() * h_x.element_size()
+    bo = h_y.numel() * h_y.element_size()
+    return {"value": round(wl.T * world / (ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 5)}
+
+
+# --------------------------------------------------------------------------- oracle legs
+def _ocfg(wl):
+    import oracle
+    return oracle.Config(hidden=wl.hidden, inter=wl.inter, num_experts=wl.num_experts,
+                         num_shared=wl.num_shared, top_k=wl.top_k,
+                         gate=oracle.GATE_SOFTMAX if wl.gate == "softmax" else oracle.GATE_SIGMOID_GROUPED,
+                         renormalize=int(wl.renormalize), n_group=wl.n_group, topk_group=wl.topk_group,
+                         routed_scale=wl.routed_scale,
+                         dtype={"f32": oracle.F32, "bf16": oracle.BF16, "fp8": oracle.FP8}[wl.dtype])
+
+
+def oracle_inputs(wl, device):
+    from moe_expert_dispatch_route_gb300 import synth
+
+    inp = synth.workload_inputs(wl, device)
+    Wn = {k: (v.cpu().float().numpy() if v.dtype == torch.bfloat16 else v.cpu().numpy())
+          for k, v in inp.items() if k.startswith("w")}
+    return inp["logits"].cpu().float().numpy(), inp["x"].cpu().float().numpy(), Wn
+
+
+def oracle_sample(wl, n_tokens: int, inputs) -> float:
+    """Seconds the single-threaded CPU oracle takes for the first n_tokens of the
+    workload, run as two ubatches like the layer."""
+    import oracle
+
+    lg, xx, Wn = inputs
+    half = (n_tokens + 1) // 2
+    t0 = time.perf_counter()
+    oracle.moe_layer(_ocfg(wl), lg[:n_tokens], xx[:n_tokens], Wn, split=half,
+                     capacity=min(wl.capacity, half) if wl.capacity else 0, align=wl.align)
+    return time.perf_counter() - t0
+
+
+def sample_size(wl, seconds: float) -> int:
+    per_token = 2 * (wl.top_k + wl.num_shared) * 3 * wl.hidden * wl.inter  # flops
+    # the oracle's plain double-precision loops run near 2.5 GFLOP/s on one core
+    return int(max(2, min(wl.T, seconds * 2.5e9 / per_token)))
+
+
+def cpu_baseline(wl):
+    n = sample_size(wl, 12.0)
+    secs = oracle_sample(wl, n, oracle_inputs(wl, "cuda"))
+    return {"value": round(n / secs, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} of {wl.T} tokens, two ubatches {(n + 1) // 2}/{n - (n + 1) // 2}, "
+                      f"single-threaded C oracle, {secs:.1f} s"}
+
+
+def run_reference(args, rank, world, local):
+    """The reference arm: the CPU oracle as it stands, a bounded sample per step."""
+    wl = workload(args)
+    if rank != 0:
+        return None, wl
+    n = sample_size(wl, 90.0 / max(1, args.steps + args.warmup))
+    inputs = oracle_inputs(wl, "cuda" if torch.cuda.is_available() else "cpu")
+    for _ in range(args.warmup):
+        oracle_sample(wl, n, inputs)
+    t = 0.0
+    for _ in range(args.steps):
+        t += oracle_sample(wl, n, inputs)
+    value = n * args.steps / t
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": wl.describe()},
+           "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                            "sample": f"first {n} of {wl.T} tokens per step, single-threaded C oracle"},
+           "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return out, wl
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_info()
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        out, _ = run_reference(args, rank, world, local)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    out, wl = run_ours(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

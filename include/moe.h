@@ -1,0 +1,271 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300: one Mixture-of-Experts layer on one GB300
+ * (sm_103a), as hand-written CUDA kernels.
+ *
+ *   moe_route      gate: top-k experts and weights per token
+ *   moe_plan       per-expert counts, aligned exclusive prefix sums, token -> row slots
+ *   moe_dispatch   gather token rows into expert-contiguous rows (fused fp8 quantisation)
+ *   moe_expert_ffn grouped gate/up GEMM -> SwiGLU -> down GEMM on the tensor cores
+ *   moe_combine    top-k weighted gather-reduce back to token order
+ *   moe_layer_dbo  all of the above on two micro-batches ("ubatches") overlapped on a
+ *                  compute stream and a comm stream (Dual-Batch Overlap)
+ *
+ * The operations follow the problem statement of the vLLM Dual-Batch Overlap pages:
+ *   [A] "[Core/DBO][1/N] Add Dual-Batch Overlap mechanism to VLLM", Purpose
+ *   [B] "[Core/DBO][2/N] Dual-Batch Overlap add DeepEP High Throughput support and
+ *       Prefill support", Purpose
+ *   [C] "[Perf] Fix DBO overlap: capture DeepEP event before yield", Purpose
+ *   [D] "DeepEP HT: full decode CUDA graphs via worst-token dispatch (whole-step +
+ *       graphed TBO)", description and commit messages
+ * The pages give no gate or FFN formulas; the arithmetic each call performs is
+ * stated beside it (the "readings").
+ *
+ * Conventions for every call
+ *  - Ownership: the caller owns every buffer, stream and workspace.  Pointers named
+ *    "device" must point to device memory of the current device.  No call allocates
+ *    device memory; the only library object is the DBO handle (a few CUDA events).
+ *  - Asynchrony: every call only enqueues work on the given stream(s) and returns;
+ *    results are valid after the stream work completes.  No call synchronises with
+ *    the host, so every call can be captured into a CUDA graph.
+ *  - Errors: argument, shape and alignment problems are detected on the host before
+ *    anything is enqueued and returned as a moe_status.  Data-dependent problems
+ *    found by a kernel (an expert id out of range, a capacity overflow, a bounded wait
+ *    that gave up) are stored in the caller's device int32 `err_flag` as a moe_status
+ *    value (the first one wins; the library never clears the flag -- zero it before
+ *    the call); the kernel then skips the offending entry, never traps.
+ *    A failed launch returns MOE_ERR_CUDA.
+ *  - Alignment: every device row buffer must start on a 16-byte boundary and rows
+ *    are packed with no stride; MOE_ERR_ALIGNMENT otherwise (never copied).
+ *  - max_ctas: upper bound on the CTAs a call's kernels may occupy (its SM budget);
+ *    <= 0 means "the whole GPU".
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, unsupported shape combination */
+    MOE_ERR_UNSUPPORTED = 2, /* valid request this build cannot serve (e.g. no sm_103a GPU) */
+    MOE_ERR_ALIGNMENT = 3,   /* a buffer or row is not 16-byte aligned */
+    MOE_ERR_WORKSPACE = 4,   /* workspace missing or smaller than the *_workspace_size query */
+    MOE_ERR_CUDA = 5,        /* a CUDA call or launch failed */
+    MOE_ERR_CAPACITY = 6,    /* device flag: an expert received more rows than `capacity` */
+    MOE_ERR_BAD_INDEX = 7,   /* device flag: an expert id outside [0, num_experts) */
+    MOE_ERR_TIMEOUT = 8      /* device flag: a bounded device-side wait gave up */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype;
+typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID_GROUPED = 1 } moe_gate;
+
+/* Shape of one layer.  E = num_experts routed experts, S = num_shared always-on
+ * experts (stored after the routed ones: expert ids E .. E+S-1), k = top_k.
+ * dtype selects the layer's storage types:
+ *   MOE_F32       x, xe, h, ye, y fp32;  weights fp32
+ *   MOE_BF16      x, xe, h, ye, y bf16;  weights bf16
+ *   MOE_FP8_E4M3  x, ye, y bf16; xe and h e4m3 with one fp32 power-of-two scale per
+ *                 1x128 group of a row; weights e4m3 with one fp32 scale per
+ *                 128x128 block.  hidden and inter must be multiples of 128.
+ * Limits: k >= 1, k + S <= 32, k <= E, E + S <= 512; grouped gate: E % n_group == 0,
+ * 2 <= E / n_group, n_group <= 32, 1 <= topk_group <= n_group,
+ * k <= topk_group * (E / n_group). */
+typedef struct {
+    int32_t hidden;       /* H */
+    int32_t inter;        /* I, intermediate size of one expert */
+    int32_t num_experts;  /* E */
+    int32_t num_shared;   /* S */
+    int32_t top_k;        /* k */
+    int32_t gate;         /* moe_gate */
+    int32_t renormalize;  /* 1: chosen weights sum to 1 (times routed_scale) */
+    int32_t n_group;      /* grouped gate only */
+    int32_t topk_group;   /* grouped gate only */
+    float routed_scale;   /* grouped gate only: multiplies the routed weights */
+    int32_t dtype;        /* moe_dtype */
+} moe_config;
+
+/* ---------------------------------------------------------------------------
+ * moe_route -- the gate.  Logits are an input: the router projection x . W_g is an
+ * ordinary dense GEMM upstream of the layer (reading; the pages name the gate kinds
+ * only through the models they serve, [C] Test Plan, [D] description).
+ *   softmax gate: the k largest logits, descending, equal logits -> lower id first;
+ *     w = the softmax probability over all E logits, or (renormalize) the softmax
+ *     over the k chosen logits.
+ *   grouped sigmoid gate: s_e = sigma(l_e) by the library's specified binary32
+ *     sigma (Cody-Waite reduced exp, degree-7 Taylor, see the design notes), choice
+ *     score c_e = s_e + bias_e; experts form n_group groups of consecutive ids; a
+ *     group scores the sum of its two best c; the topk_group best groups are kept
+ *     (equal -> lower group id); the k best c inside them are chosen (equal -> lower
+ *     id); w = sigmoid(l) of the chosen (no bias), / their sum if renormalize, times
+ *     routed_scale.  Selection is bit-reproducible; weights are fp32.
+ * logits   device fp32 [T][E], row-major.
+ * bias     device fp32 [E] or NULL (grouped gate only; NULL = 0).
+ * topk_ids device int32 [T][k] (out), descending score order.
+ * topk_w   device fp32 [T][k] (out).
+ * T = 0 is a no-op. */
+MOE_API moe_status moe_route(const moe_config* cfg, int32_t T, const float* logits, const float* bias,
+                     int32_t* topk_ids, float* topk_w, int32_t max_ctas, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_plan -- per-expert counts, aligned exclusive prefix sums and the row ("slot")
+ * of every (token, choice) pair: a stable counting sort.  Per-expert counts stay in
+ * device memory and a static worst-case capacity keeps shapes fixed for graph
+ * capture ([D] description: worst-token dispatch, device-side counts; the
+ * BatchedExperts vs Standard activation formats of its commit messages).
+ * Entry (t, j) is expert topk_ids[t][j] for j < k and shared expert E + (j - k) for
+ * k <= j < k + S.  Rows of one expert are in (t, j) order.
+ *   capacity == 0 ("exact", contiguous): expert e owns rows [offsets[e],
+ *     offsets[e] + counts[e]); offsets[e+1] = offsets[e] + counts[e] rounded up to a
+ *     multiple of `align` (>= 1); offsets[E+S] = rows used.
+ *   capacity  > 0 ("worst-token", per-expert padded): expert e owns rows
+ *     [e*capacity, (e+1)*capacity); counts[e] = rows placed; an entry ranked
+ *     >= capacity gets slot -1 and sets MOE_ERR_CAPACITY (never dropped silently).
+ *     capacity = T is the single-GPU worst case (a token picks an expert once).
+ * topk_ids device int32 [T][k].
+ * counts   device int32 [E+S] (out); offsets device int32 [E+S+1] (out).
+ * slot_of  device int32 [T][k+S] (out): row of each entry, -1 if not placed.
+ * token_of device int32 [moe_plan_rows(...)] (out): token of each row, -1 = padding.
+ * err_flag device int32 (required): MOE_ERR_BAD_INDEX / MOE_ERR_CAPACITY.
+ * ws       device scratch of moe_plan_workspace_size(cfg, T) bytes (may be NULL when
+ *          that is 0). */
+MOE_API size_t moe_plan_rows(const moe_config* cfg, int32_t T, int32_t capacity, int32_t align);
+MOE_API size_t moe_plan_workspace_size(const moe_config* cfg, int32_t T);
+MOE_API moe_status moe_plan(const moe_config* cfg, int32_t T, const int32_t* topk_ids, int32_t capacity,
+                    int32_t align, int32_t* counts, int32_t* offsets, int32_t* slot_of,
+                    int32_t* token_of, int32_t* err_flag, void* ws, size_t ws_bytes,
+                    int32_t max_ctas, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_dispatch -- on-device analogue of the all-to-all dispatch ([A] Purpose):
+ * xe[slot_of[t][j]] = x[t] for every placed entry (slot >= 0).  FP8 layers quantise
+ * each 1x128 group of the bf16 row with the power-of-two scale 2^s, s the smallest
+ * integer with amax <= 448 * 2^s (amax = 0 -> s = 0), e4m3 round-to-nearest-even:
+ * xe_scale[row][g] = 2^s.  Rows no entry maps to are not written.
+ * x        device [T][H]: fp32 (MOE_F32) or bf16.
+ * xe       device [rows][H]: fp32 / bf16 / e4m3 (out).
+ * xe_scale device fp32 [rows][H/128] (out, FP8 only; else NULL). */
+MOE_API moe_status moe_dispatch(const moe_config* cfg, int32_t T, const void* x, const int32_t* slot_of,
+                        void* xe, float* xe_scale, int32_t max_ctas, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_expert_ffn -- every expert's SwiGLU FFN on its rows (the grouped expert GEMMs
+ * and the fused activation the pages name: DeepGEMM / batched Triton MoE GEMM with
+ * act_and_mul / silu_mul_fp8_quant, [A] discussion, [B] Purpose):
+ *   g|u = xe[r] . W13[e]^T   (W13 rows 0..I-1 gate, I..2I-1 up),
+ *   h   = silu(g) * u        stored as the activation type (fp8: 1x128 scales),
+ *   ye[r] = h . W2[e]^T      stored as fp32 (MOE_F32) or bf16,
+ * for r in [offsets[e], offsets[e] + counts[e]), e in [0, E+S); fp32 accumulation.
+ * Tile work is derived from the device counts/offsets: no host synchronisation.
+ * Rows outside the used ranges are neither read into results nor written.
+ * counts, offsets device int32 [E+S], [E+S+1] (from moe_plan).
+ * max_rows  rows of xe / ye (moe_plan_rows); a range beyond it sets MOE_ERR_BAD_INDEX.
+ * w13      device [E+S][2I][H]; w2 device [E+S][H][I]; fp32 / bf16 / e4m3.
+ * w13_scale device fp32 [E+S][2I/128][H/128]; w2_scale [E+S][H/128][I/128] (FP8 only).
+ * ye       device [max_rows][H] (out).
+ * ws       device scratch of moe_ffn_workspace_size(cfg, max_rows) bytes.
+ * err_flag device int32 or NULL. */
+MOE_API size_t moe_ffn_workspace_size(const moe_config* cfg, int64_t max_rows);
+MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const int32_t* counts, const int32_t* offsets,
+                          int64_t max_rows, const void* xe, const float* xe_scale, const void* w13,
+                          const float* w13_scale, const void* w2, const float* w2_scale, void* ye,
+                          void* ws, size_t ws_bytes, int32_t* err_flag, int32_t max_ctas,
+                          moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_combine -- on-device analogue of the all-to-all combine ([A] Purpose):
+ * y[t] = sum_{j<k} topk_w[t][j] * ye[slot_of[t][j]] + sum_{s<S} ye[slot_of[t][k+s]],
+ * accumulated in fp32 in (j, then s) order, rounded once to the output type; entries
+ * with slot -1 contribute nothing.  Deterministic (no atomics).
+ * ye device [rows][H] fp32/bf16; topk_w device fp32 [T][k]; y device [T][H] (out). */
+MOE_API moe_status moe_combine(const moe_config* cfg, int32_t T, const void* ye, const float* topk_w,
+                       const int32_t* slot_of, void* y, int32_t max_ctas, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Dual-Batch Overlap.  The batch is split into two ubatches, tokens [0, s) and
+ * [s, T).  One ubatch's route / plan / dispatch and combine run on the comm stream
+ * while the other's expert FFN runs on the compute stream ([A] Purpose); every
+ * event a comm step waits on is recorded on the compute stream right after the
+ * producing kernel, before the other ubatch's compute is enqueued, so it covers
+ * only that ubatch's compute tail ([C] Purpose); the comm stream is joined back to
+ * the compute stream before the call returns, so no comm work is left in flight
+ * ([D] commit messages: dispatch and combine joined to the compute stream).  The
+ * enqueue order is one fixed schedule: no host threads and no yields are needed
+ * for a single layer.
+ */
+typedef struct moe_dbo_handle moe_dbo_handle;
+MOE_API moe_status moe_dbo_create(moe_dbo_handle** out);
+MOE_API void moe_dbo_destroy(moe_dbo_handle* h);
+
+/* Everything moe_layer_dbo reads and writes.  Inputs: logits fp32 [T][E], bias
+ * (nullable), x [T][H], the weights and scales as for moe_expert_ffn.  Outputs:
+ * y [T][H], topk_ids int32 [T][k], topk_w fp32 [T][k], err_flag (nullable: then a
+ * flag inside the workspace is used).  workspace: moe_layer_workspace_size bytes,
+ * 256-byte aligned, holding both ubatches' plans, xe, h and ye. */
+typedef struct {
+    const float* logits;
+    const float* bias;
+    const void* x;
+    const void* w13;
+    const float* w13_scale;
+    const void* w2;
+    const float* w2_scale;
+    void* y;
+    int32_t* topk_ids;
+    float* topk_w;
+    int32_t* err_flag;
+    void* workspace;
+    size_t workspace_bytes;
+} moe_layer_args;
+
+/* Workspace for moe_layer_dbo with T tokens (either split or not). */
+MOE_API size_t moe_layer_workspace_size(const moe_config* cfg, int32_t T, int32_t capacity, int32_t align);
+
+/* The whole layer.
+ * split     0 -> ceil(T/2); s in [1, T) -> ubatches [0, s), [s, T); s >= T -> no split.
+ *           T < min_tokens also runs unsplit (never an empty ubatch, [B] commit list).
+ * capacity  0 = exact layout; > 0 = worst-token layout with that many rows per expert
+ *           per ubatch (must be >= the ubatch's token count for no overflow).
+ * comm_sms  CTAs given to route/plan/dispatch/combine; the expert FFN gets the
+ *           remaining SMs.  0 = no split of the GPU.
+ * compute, comm  the two streams; comm == compute runs the identical two-ubatch
+ *           schedule serialised on one stream.
+ * The call resets *err_flag to 0 on the compute stream before its kernels run. */
+MOE_API moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_layer_args* args,
+                         int32_t T, int32_t split, int32_t min_tokens, int32_t capacity,
+                         int32_t align, int32_t comm_sms, moe_stream_t compute, moe_stream_t comm);
+
+/* The enqueue schedule moe_layer_dbo follows, for inspection (host only, no GPU
+ * needed).  Writes up to max_ops records of 4 int32 each: {stream (0 compute,
+ * 1 comm), op (see MOE_OP_*), ubatch (0/1, -1 = none), event id (record/wait) or -1}
+ * and returns the number of records.  two_ubatches = 0 gives the unsplit schedule. */
+enum {
+    MOE_OP_ROUTE = 0,
+    MOE_OP_PLAN = 1,
+    MOE_OP_DISPATCH = 2,
+    MOE_OP_FFN = 3,
+    MOE_OP_COMBINE = 4,
+    MOE_OP_RECORD = 5,
+    MOE_OP_WAIT = 6
+};
+MOE_API int32_t moe_dbo_schedule(int32_t two_ubatches, int32_t* ops, int32_t max_ops);
+
+MOE_API const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

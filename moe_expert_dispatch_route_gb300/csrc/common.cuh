@@ -1,0 +1,72 @@
+// Device-side helpers shared by the kernels of libmoe_gb300.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kQG = 128;            // FP8 quantisation group / block edge
+constexpr int kMaxExperts = 512;    // E + S
+constexpr int kMaxSlotsPerToken = 32;  // k + S
+
+// Stores `code` into the caller's device error flag unless an earlier error is there.
+__device__ __forceinline__ void set_err(int32_t* flag, int32_t code) {
+    if (flag) atomicCAS(reinterpret_cast<int*>(flag), 0, code);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Exponent s of the power-of-two FP8 scale 2^s: the smallest integer with
+// amax <= 448 * 2^s (448 = 0.875 * 2^9); amax == 0 gives 0.
+__device__ __forceinline__ int fp8_scale_exp(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int e;
+    float f = frexpf(amax, &e);
+    return (f <= 0.875f) ? e - 9 : e - 8;
+}
+
+// Two floats -> two e4m3 codes (round to nearest even, saturating to +-448).
+__device__ __forceinline__ uint16_t f2_to_e4m3x2(float a, float b) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float e4m3_to_f(uint8_t c) {
+    __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+    return __half2float(__half(hr));
+}
+
+__device__ __forceinline__ float bf16_bits_to_f(uint16_t b) {
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f_to_bf16_bits(float f) {
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return (uint32_t)f_to_bf16_bits(lo) | ((uint32_t)f_to_bf16_bits(hi) << 16);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+}  // namespace moe

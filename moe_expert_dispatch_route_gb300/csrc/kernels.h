@@ -1,0 +1,66 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+// Arguments are already validated by the caller; each launcher only enqueues.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int cc_major, cc_minor;
+    size_t smem_optin;
+};
+const DeviceInfo& device_info();
+moe_status check_config(const moe_config* c);  // shape limits and row alignment
+bool aligned16(const void* p);
+
+// route.cu
+cudaError_t launch_route(const moe_config& c, int T, const float* logits, const float* bias,
+                         int32_t* ids, float* w, int grid_cap, cudaStream_t st);
+
+// plan.cu
+int plan_tokens_per_chunk(const moe_config& c);
+int plan_num_chunks(const moe_config& c, int T);
+cudaError_t launch_plan(const moe_config& c, int T, const int32_t* ids, int capacity, int align,
+                        int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* token_of,
+                        int32_t* err, int32_t* hist_ws, int grid_cap, cudaStream_t st);
+
+// dispatch.cu / combine.cu
+cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int32_t* slot_of,
+                            void* xe, float* xe_scale, int grid_cap, cudaStream_t st);
+cudaError_t launch_combine(const moe_config& c, int T, const void* ye, const float* w,
+                           const int32_t* slot_of, void* y, int grid_cap, cudaStream_t st);
+
+// FFN: scratch = h [max_rows][I] (+ fp8 scales) followed by the kernels' own scratch.
+size_t ffn_scratch_bytes(const moe_config& c, int64_t max_rows);
+struct FfnArgs {
+    const int32_t* counts;
+    const int32_t* offsets;
+    int64_t max_rows;
+    const void* xe;
+    const float* xe_scale;
+    const void* w13;
+    const float* w13_scale;
+    const void* w2;
+    const float* w2_scale;
+    void* ye;
+    void* ws;
+    int32_t* err;
+    int reverse;  // walk experts in descending order (L2 reuse across ubatches)
+};
+cudaError_t launch_ffn(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
+
+// ffn_simt.cu: portable CUDA-core grouped GEMM (fp32 layers, and any layer on request)
+cudaError_t launch_ffn_simt(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int elt_bytes(int dtype) { return dtype == MOE_F32 ? 4 : dtype == MOE_BF16 ? 2 : 1; }
+// bytes of one element of x / ye / y (fp8 layers keep bf16 there)
+inline int io_bytes(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
+
+}  // namespace moe

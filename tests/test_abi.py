@@ -1,0 +1,130 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every symbol moe.h declares, rejects bad arguments before touching a
+device, sizes its workspaces, and its Dual-Batch Overlap schedule keeps the
+dependency rules."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_expert_dispatch_route_gb300 import binding as B
+from moe_expert_dispatch_route_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        src = f.read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["moe_route", "moe_plan", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer_dbo",
+              "moe_dbo_create", "moe_dbo_destroy", "moe_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = B.lib()
+    declared = _declared()
+    for n in declared:
+        assert hasattr(L, n), n
+    assert set(declared) <= set(B.EXPORTS)
+
+
+def test_status_strings():
+    assert B.moe_status_string(0) == "ok"
+    assert "capacity" in B.moe_status_string(6)
+    assert B.moe_status_string(99) == "unknown status"
+
+
+def test_invalid_arguments_rejected_on_host():
+    L = B.lib()
+    cfg = B.config_of(W.QWEN3_DECODE)
+    bad = B.config_of(W.QWEN3_DECODE)
+    bad.top_k = 0
+    assert L.moe_route(ctypes.byref(bad), 4, 16, None, 16, 16, 0, None) == 1
+    assert L.moe_route(ctypes.byref(cfg), 4, None, None, 16, 16, 0, None) == 1
+    assert L.moe_route(ctypes.byref(cfg), 0, None, None, None, None, 0, None) == 0  # empty batch
+    assert L.moe_dispatch(ctypes.byref(cfg), 4, 8, 16, 16, None, 0, None) == 3        # misaligned x
+    g = B.config_of(W.DSV3)
+    g.n_group = 7  # 256 % 7 != 0
+    assert L.moe_route(ctypes.byref(g), 4, 16, None, 16, 16, 0, None) == 1
+    f = B.config_of(W.QWEN3_PREFILL)
+    f.hidden = 2000  # fp8 needs multiples of 128
+    assert L.moe_dispatch(ctypes.byref(f), 4, 16, 16, 16, 16, 0, None) == 3
+    # plan: workspace required when the batch spans several chunks
+    assert B.moe_plan_workspace_size(cfg, 100000) > 0
+    assert L.moe_plan(ctypes.byref(cfg), 100000, 16, 0, 128, 16, 16, 16, 16, 16, None, 0, 0, None) == 4
+    # layer: workspace too small
+    h = ctypes.c_void_p(1)
+    args = B.MoeLayerArgs(16, None, 16, 16, None, 16, None, 16, 16, 16, None, 256, 1024)
+    assert L.moe_layer_dbo(h, ctypes.byref(cfg), ctypes.byref(args), 256, 0, 4, 0, 128, 0, None, None) == 4
+
+
+def test_plan_rows_and_workspace_sizes():
+    cfg = B.config_of(W.DSV2LITE)
+    NE, kk = 66, 8
+    assert B.moe_plan_rows(cfg, 512, 0, 128) == 512 * kk + NE * 127
+    assert B.moe_plan_rows(cfg, 512, 256, 128) == NE * 256
+    assert B.moe_plan_rows(cfg, 512, 0, 1) == 512 * kk
+    assert B.moe_plan_workspace_size(cfg, 64) == 0   # one chunk: no scratch
+    ws = B.moe_layer_workspace_size(cfg, 4096, 0, 128)
+    assert ws > 2 * B.moe_plan_rows(cfg, 4096, 0, 128) * 2048 * 2 * 2  # xe + ye per ubatch
+    assert B.moe_ffn_workspace_size(B.config_of(W.QWEN3_PREFILL), 1000) >= 1000 * 768
+
+
+def _events(sched):
+    """For each event id: (stream, position) of its record."""
+    return {ev: (st, i) for i, (st, op, ub, ev) in enumerate(sched) if op == 5}
+
+
+def test_dbo_schedule_dependencies():
+    s = B.moe_dbo_schedule(True)
+    ops = [(st, B.OPS[op], ub, ev) for st, op, ub, ev in s]
+    rec = _events(s)
+
+    def pos(name, ub):
+        return next(i for i, o in enumerate(ops) if o[1] == name and o[2] == ub)
+
+    # dispatch/route/plan and combine on the comm stream, experts on compute
+    for name in ("route", "plan", "dispatch", "combine"):
+        for ub in (0, 1):
+            assert ops[pos(name, ub)][0] == 1
+    assert ops[pos("ffn", 0)][0] == 0 and ops[pos("ffn", 1)][0] == 0
+
+    def waits_before(i, stream):
+        return [o[3] for o in ops[:i] if o[0] == stream and o[1] == "wait"]
+
+    # ffn(u) waits for dispatch(u): the event it waits on is recorded right after dispatch(u)
+    for ub in (0, 1):
+        evs = waits_before(pos("ffn", ub), 0)
+        ev = evs[-1]
+        st, at = rec[ev]
+        assert st == 1 and ops[at - 1][1] == "dispatch" and ops[at - 1][2] == ub
+    # combine(0) waits on an event recorded right after ffn(0) -- BEFORE ffn(1) is
+    # enqueued, so it does not cover the other ubatch's compute
+    ev = waits_before(pos("combine", 0), 1)[-1]
+    st, at = rec[ev]
+    assert st == 0 and ops[at - 1][1] == "ffn" and ops[at - 1][2] == 0
+    assert at < pos("ffn", 1)
+    # the comm-side work of ubatch 1 is not behind ffn(0): no wait on the comm stream
+    # between the fork and dispatch(1) refers to a compute-stream event other than the fork
+    for e in waits_before(pos("dispatch", 1), 1):
+        assert rec[e][1] < pos("ffn", 0)
+    # join: the last op makes the compute stream wait for the comm stream's last record
+    last = ops[-1]
+    assert last[0] == 0 and last[1] == "wait" and rec[last[3]][0] == 1
+    assert max(i for i, o in enumerate(ops) if o[0] == 1) == rec[last[3]][1]
+    # every ubatch runs the same steps (the two ubatches perform equal numbers of yields)
+    for name in ("route", "plan", "dispatch", "ffn", "combine"):
+        assert sum(1 for o in ops if o[1] == name) == 2
+
+
+def test_unsplit_schedule_is_one_stream():
+    s = B.moe_dbo_schedule(False)
+    assert [B.OPS[o[1]] for o in s] == ["route", "plan", "dispatch", "ffn", "combine"]
+    assert all(o[0] == 0 for o in s)
