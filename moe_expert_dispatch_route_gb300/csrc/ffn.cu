@@ -1,5 +1,8 @@
 // moe_expert_ffn: chooses the expert-FFN kernels for a layer and owns the layout of
 // their scratch memory (h, the SwiGLU output, and its fp8 scales).
+#include <stdlib.h>
+#include <string.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -11,7 +14,19 @@ size_t ffn_scratch_bytes(const moe_config& c, int64_t max_rows) {
     return b;
 }
 
+// MOE_FFN_IMPL=simt selects the CUDA-core kernels for every layer (a second,
+// independent implementation to compare the tensor-core kernels with).
+static bool force_simt() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("MOE_FFN_IMPL");
+        v = (e && strcmp(e, "simt") == 0) ? 1 : 0;
+    }
+    return v == 1;
+}
+
 cudaError_t launch_ffn(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st) {
+    if (!force_simt() && ffn_tc_supported(c)) return launch_ffn_tc(c, a, grid_cap, st);
     return launch_ffn_simt(c, a, grid_cap, st);
 }
 

@@ -1,0 +1,454 @@
+// Grouped expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Two persistent, warp-specialised kernels, one CTA per SM:
+//   up   : acc[128 x 256] = xe[rows] . [W13 gate rows n0..n0+127 | up rows I+n0..]^T,
+//          epilogue h = silu(g) * u -> bf16 h[rows][n0..n0+127]
+//   down : acc[128 x 256] = h[rows] . W2[e][n0..n0+255]^T, epilogue -> bf16 ye
+// A tile = 128 rows of one expert's segment (rows past the segment are computed and
+// discarded), B tile = 256 weight rows; k-blocks of 64 bf16 (one 128-byte swizzle
+// row).  Tiles (expert, n-block, m-block) are derived on the device from counts and
+// offsets, so no host synchronisation is needed and the launch is graph-capturable.
+//
+// Roles (192 threads):
+//   warp 0 (one lane)  TMA producer: 4-stage ring of {A 16 KB, B 32 KB}
+//   warp 1 (one lane)  MMA issuer: tcgen05.mma M=128 N=256 K=16 into a TMEM
+//                      accumulator, double buffered (2 x 256 of 512 columns)
+//   warps 2..5         epilogue: tcgen05.ld of the warp's 32 TMEM lanes (one row per
+//                      thread), activation, stores of the row's columns
+// Every wait is bounded: after kWaitTimeoutNs a role raises a CTA-wide abort flag,
+// stores MOE_ERR_TIMEOUT, drains its own outstanding copies / MMAs, and the CTA frees
+// its TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;  // full, empty, tmem full, tmem empty, drain
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kStages * kStageBytes + kNumBars * 8 + 16 + 3 * (kMaxExperts + 1) * sizeof(int);
+
+struct TcParams {
+    CUtensorMap tmA;  // activations [max_rows][K] bf16
+    CUtensorMap tmB;  // weights [NE * NB][K] bf16
+    const int32_t* counts;
+    const int32_t* offsets;
+    int NE, K, kblocks;
+    int NB;   // weight rows per expert
+    int ntn;  // n-blocks per expert
+    int I, H;
+    int64_t max_rows;
+    void* out;
+    int32_t* err;
+    int reverse;
+};
+
+struct Smem {
+    uint8_t* stages;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* tfull;
+    uint64_t* tempty;
+    uint64_t* drain;
+    uint32_t* tmem_base;
+    volatile int* abort;
+    int* tstart;
+    int* cnt;
+    int* off;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw) {
+    Smem s;
+    uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    s.stages = p;
+    p += (size_t)kStages * kStageBytes;
+    s.full = reinterpret_cast<uint64_t*>(p);
+    s.empty = s.full + kStages;
+    s.tfull = s.empty + kStages;
+    s.tempty = s.tfull + 2;
+    s.drain = s.tempty + 2;
+    s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.abort = reinterpret_cast<volatile int*>(s.tmem_base + 1);
+    s.tstart = reinterpret_cast<int*>(s.tmem_base + 4);
+    s.cnt = s.tstart + (kMaxExperts + 1);
+    s.off = s.cnt + (kMaxExperts + 1);
+    return s;
+}
+
+__device__ __forceinline__ void fail(const Smem& s, int32_t* err) {
+    set_err(err, MOE_ERR_TIMEOUT);
+    *s.abort = 1;
+}
+
+struct Tile {
+    int e, mt, nt, rows;
+    int row0;
+};
+
+__device__ __forceinline__ Tile decode_tile(const TcParams& p, const Smem& s, int total, int lin) {
+    const int tile = p.reverse ? total - 1 - lin : lin;
+    int lo = 0, hi = p.NE - 1;
+    while (lo < hi) {  // largest e with tstart[e] <= tile
+        const int mid = (lo + hi + 1) >> 1;
+        if (s.tstart[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    Tile t;
+    t.e = lo;
+    const int local = tile - s.tstart[lo];
+    const int cnt = s.cnt[lo];
+    const int mtiles = (cnt + kBM - 1) / kBM;
+    t.nt = local / mtiles;  // n-major within an expert: consecutive CTAs share B
+    t.mt = local % mtiles;
+    t.row0 = s.off[lo] + t.mt * kBM;
+    t.rows = min(kBM, cnt - t.mt * kBM);
+    return t;
+}
+
+// One warp: copies counts/offsets into shared memory and scans the tile counts.
+__device__ void scan_tiles(const TcParams& p, const Smem& s) {
+    const int lane = threadIdx.x & 31;
+    const int per = (p.NE + 31) / 32;
+    int vals[16];
+    int sum = 0;
+    for (int i = 0; i < per; ++i) {
+        const int e = lane * per + i;
+        int v = 0;
+        if (e < p.NE) {
+            int cnt = __ldg(p.counts + e);
+            const int off = __ldg(p.offsets + e);
+            if (cnt < 0 || off < 0 || (int64_t)off + cnt > p.max_rows) {
+                set_err(p.err, MOE_ERR_BAD_INDEX);
+                cnt = 0;
+            }
+            s.cnt[e] = cnt;
+            s.off[e] = off;
+            v = (cnt + kBM - 1) / kBM * p.ntn;
+        }
+        vals[i] = v;
+        sum += v;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    int run = incl - sum;
+    for (int i = 0; i < per; ++i) {
+        const int e = lane * per + i;
+        if (e < p.NE) s.tstart[e] = run;
+        run += vals[i];
+    }
+    if (lane == 31) s.tstart[p.NE] = incl;
+}
+
+template <bool kUp>
+__device__ void producer(const TcParams& p, const Smem& s, int total) {
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t pending = 0, pend_par = 0;  // per stage: a load in flight, and its phase parity
+    bool ok = true;
+    for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
+        const Tile t = decode_tile(p, s, total, lin);
+        int b0, b1;
+        if (kUp) {
+            b0 = t.e * p.NB + t.nt * 128;
+            b1 = t.e * p.NB + p.I + t.nt * 128;
+        } else {
+            b0 = t.e * p.NB + t.nt * kBN;
+            b1 = b0 + 128;
+        }
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (!tc::mbar_wait(&s.empty[stage], phase ^ 1u, s.abort)) {
+                ok = false;
+                break;
+            }
+            uint8_t* a = s.stages + (size_t)stage * kStageBytes;
+            uint8_t* b = a + kABytes;
+            tc::mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
+            tc::tma_load_2d(a, &p.tmA, &s.full[stage], kb * kBK, t.row0);
+            tc::tma_load_2d(b, &p.tmB, &s.full[stage], kb * kBK, b0);
+            tc::tma_load_2d(b + kBBytes / 2, &p.tmB, &s.full[stage], kb * kBK, b1);
+            pending |= 1u << stage;
+            pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        fail(s, p.err);
+        // let the copies already issued land before the CTA exits
+        for (int st = 0; st < kStages; ++st)
+            if ((pending >> st) & 1u) {
+                const uint64_t t0 = tc::globaltimer();
+                while (!tc::mbar_try_wait(&s.full[st], (pend_par >> st) & 1u) &&
+                       tc::globaltimer() - t0 < tc::kWaitTimeoutNs) {
+                }
+            }
+    }
+}
+
+__device__ void mma_issuer(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
+    int stage = 0;
+    uint32_t phase = 0;
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
+    for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
+        if (!tc::mbar_wait(&s.tempty[buf], acc_phase ^ 1u, s.abort)) {
+            ok = false;
+            break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * kBN);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (!tc::mbar_wait(&s.full[stage], phase, s.abort)) {
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            const uint32_t a_addr = tc::smem_u32(s.stages + (size_t)stage * kStageBytes);
+            const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                tc::mma_bf16(d, tc::desc_sw128_kmajor(a_addr + kk * 32), tc::desc_sw128_kmajor(b_addr + kk * 32),
+                             idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc::mma_commit(&s.empty[stage]);  // frees the smem stage once these MMAs finish
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        tc::mma_commit(&s.tfull[buf]);  // accumulator ready for the epilogue
+        buf ^= 1;
+        if (buf == 0) acc_phase ^= 1u;
+    }
+    if (!ok) fail(s, p.err);
+    // drain: every MMA issued above has completed before TMEM is released
+    tc::mma_commit(s.drain);
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(s.drain, 0) && tc::globaltimer() - t0 < tc::kWaitTimeoutNs) {
+    }
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+template <bool kUp>
+__device__ void epilogue(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    for (int lin = blockIdx.x; lin < total; lin += gridDim.x) {
+        const Tile t = decode_tile(p, s, total, lin);
+        if (!tc::mbar_wait(&s.tfull[buf], acc_phase, s.abort)) {
+            fail(s, p.err);
+            break;
+        }
+        tc::tc_fence_after();
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN);
+        const bool valid = r < t.rows;
+        const int64_t row = (int64_t)t.row0 + r;
+        if (kUp) {
+            uint16_t* hrow = static_cast<uint16_t*>(p.out) + row * p.I + t.nt * 128;
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+                uint32_t g[32], u[32];
+                tc::tmem_ld32(tb + c, g);
+                tc::tmem_ld32(tb + 128 + c, u);
+                tc::tmem_wait_ld();
+                if (valid) {
+                    uint4 v[4];
+                    uint32_t* w = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                           silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+                    uint4* dst = reinterpret_cast<uint4*>(hrow + c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = v[i];
+                }
+            }
+        } else {
+            uint16_t* yrow = static_cast<uint16_t*>(p.out) + row * p.H + t.nt * kBN;
+#pragma unroll 1
+            for (int c = 0; c < kBN; c += 32) {
+                uint32_t a[32];
+                tc::tmem_ld32(tb + c, a);
+                tc::tmem_wait_ld();
+                if (valid) {
+                    uint4 v[4];
+                    uint32_t* w = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                    uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = v[i];
+                }
+            }
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&s.tempty[buf]);
+        buf ^= 1;
+        if (buf == 0) acc_phase ^= 1u;
+    }
+}
+
+template <bool kUp>
+__global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem s = carve(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            tc::mbar_init(&s.full[i], 1);
+            tc::mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&s.tfull[i], 1);
+            tc::mbar_init(&s.tempty[i], 4);
+        }
+        tc::mbar_init(s.drain, 1);
+        *s.abort = 0;
+        tc::fence_barrier_init();
+        tc::prefetch_tmap(&p.tmA);
+        tc::prefetch_tmap(&p.tmB);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(s.tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (warp == 2) scan_tiles(p, s);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem_base = *s.tmem_base;
+    const int total = s.tstart[p.NE];
+
+    if (warp == 0) {
+        if (lane == 0) producer<kUp>(p, s, total);
+    } else if (warp == 1) {
+        if (lane == 0) mma_issuer(p, s, total, tmem_base);
+    } else {
+        epilogue<kUp>(p, s, total, tmem_base);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 2-D K-major bf16 matrix [rows][inner], box 64 x 128 with the 128-byte swizzle.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, 128};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kUp>
+cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
+    static int configured_dev = -1;
+    const int dev = device_info().device;
+    if (configured_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(ffn_tc_bf16_kernel<kUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    ffn_tc_bf16_kernel<kUp><<<grid, kThreads, kSmemBytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool ffn_tc_supported(const moe_config& c) {
+    const DeviceInfo& d = device_info();
+    return c.dtype == MOE_BF16 && d.cc_major == 10 && c.hidden % kBN == 0 && c.inter % 128 == 0 &&
+           c.hidden % kBK == 0 && d.smem_optin >= kSmemBytes && encode_fn() != nullptr;
+}
+
+cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st) {
+    const int NE = c.num_experts + c.num_shared;
+    const int H = c.hidden, I = c.inter;
+    int grid = device_info().num_sms;
+    if (grid > grid_cap) grid = grid_cap;
+    if (grid < 1) grid = 1;
+    void* h = a.ws;
+    TcParams up{};
+    if (!make_map_bf16(&up.tmA, a.xe, (uint64_t)H, (uint64_t)a.max_rows) ||
+        !make_map_bf16(&up.tmB, a.w13, (uint64_t)H, (uint64_t)NE * 2 * I))
+        return cudaErrorInvalidValue;
+    up.counts = a.counts;
+    up.offsets = a.offsets;
+    up.NE = NE;
+    up.K = H;
+    up.kblocks = H / kBK;
+    up.NB = 2 * I;
+    up.ntn = I / 128;
+    up.I = I;
+    up.H = H;
+    up.max_rows = a.max_rows;
+    up.out = h;
+    up.err = a.err;
+    up.reverse = a.reverse;
+    TcParams dn = up;
+    if (!make_map_bf16(&dn.tmA, h, (uint64_t)I, (uint64_t)a.max_rows) ||
+        !make_map_bf16(&dn.tmB, a.w2, (uint64_t)I, (uint64_t)NE * H))
+        return cudaErrorInvalidValue;
+    dn.K = I;
+    dn.kblocks = I / kBK;
+    dn.NB = H;
+    dn.ntn = H / kBN;
+    dn.out = a.ye;
+    cudaError_t e = launch_one<true>(up, grid, st);
+    if (e != cudaSuccess) return e;
+    return launch_one<false>(dn, grid, st);
+}
+
+}  // namespace moe

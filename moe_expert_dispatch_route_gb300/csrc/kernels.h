@@ -58,6 +58,10 @@ cudaError_t launch_ffn(const moe_config& c, const FfnArgs& a, int grid_cap, cuda
 // ffn_simt.cu: portable CUDA-core grouped GEMM (fp32 layers, and any layer on request)
 cudaError_t launch_ffn_simt(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
 
+// ffn_tc.cu: tcgen05 / TMEM / TMA grouped GEMM (bf16 layers)
+bool ffn_tc_supported(const moe_config& c);
+cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int elt_bytes(int dtype) { return dtype == MOE_F32 ? 4 : dtype == MOE_BF16 ? 2 : 1; }
 // bytes of one element of x / ye / y (fp8 layers keep bf16 there)
