@@ -150,6 +150,30 @@ MOE_API moe_status moe_plan(const moe_config* cfg, int32_t T, const int32_t* top
                     int32_t max_ctas, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_plan_noalloc -- moe_plan for callers that cannot allocate device memory:
+ * code that runs where cudaMalloc is unavailable or forbidden (inside a CUDA-graph
+ * capture with a locked memory pool, under an allocator that owns all device memory,
+ * in a plugin that receives only tensor pointers), or that cannot size a workspace
+ * ahead of time.  The pages have no counterpart to this call; it is a convenience of
+ * this library.
+ * Same arguments, results and errors as moe_plan, minus the workspace.  The plan's
+ * scratch (per-chunk expert histograms) is a fixed 256 KiB array inside the
+ * library's device memory, held by every GPU that loads the library until the
+ * process exits.  Limit: moe_plan_workspace_size(cfg, T) <= 262144 bytes, i.e.
+ * ceil(T / floor(4096 / (k+S))) * (E+S) <= 65536; a larger T returns
+ * MOE_ERR_WORKSPACE before anything is enqueued (MOE_DEBUG=1 prints why).
+ * The first call on a device that needs the scratch looks up the array's device
+ * address with that device current; make that first call before any stream capture.
+ * All calls share the one array, so calls whose kernels overlap on the GPU (on
+ * different streams without ordering) race; calls ordered on one stream do not.
+ * The array keeps the last call's contents; every entry a call reads is written
+ * earlier in that same call, so nothing needs clearing.  No call allocates. */
+MOE_API moe_status moe_plan_noalloc(const moe_config* cfg, int32_t T, const int32_t* topk_ids,
+                                    int32_t capacity, int32_t align, int32_t* counts, int32_t* offsets,
+                                    int32_t* slot_of, int32_t* token_of, int32_t* err_flag,
+                                    int32_t max_ctas, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * moe_dispatch -- on-device analogue of the all-to-all dispatch ([A] Purpose):
  * xe[slot_of[t][j]] = x[t] for every placed entry (slot >= 0).  FP8 layers quantise
  * each 1x128 group of the bf16 row with the power-of-two scale 2^s, s the smallest

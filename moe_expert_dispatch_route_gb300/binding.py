@@ -67,6 +67,7 @@ _SIGS = {
     "moe_plan_rows": (_SZ, [_CFG, _I32, _I32, _I32]),
     "moe_plan_workspace_size": (_SZ, [_CFG, _I32]),
     "moe_plan": (_I32, [_CFG, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _I32, _P]),
+    "moe_plan_noalloc": (_I32, [_CFG, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P]),
     "moe_dispatch": (_I32, [_CFG, _I32, _P, _P, _P, _P, _I32, _P]),
     "moe_ffn_workspace_size": (_SZ, [_CFG, _I64]),
     "moe_expert_ffn": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _I32, _P]),
@@ -145,6 +146,14 @@ def moe_plan(cfg, T, topk_ids, capacity, align, counts, offsets, slot_of, token_
     _check(lib().moe_plan(ctypes.byref(cfg), T, _ptr(topk_ids), capacity, align, _ptr(counts), _ptr(offsets),
                           _ptr(slot_of), _ptr(token_of), _ptr(err_flag), _ptr(ws), ws_bytes, max_ctas,
                           _stream(stream)), "moe_plan")
+
+
+def moe_plan_noalloc(cfg, T, topk_ids, capacity, align, counts, offsets, slot_of, token_of, err_flag,
+                     max_ctas=0, stream=None):
+    """moe_plan without a workspace (scratch lives in the library; see moe.h for the limit)."""
+    _check(lib().moe_plan_noalloc(ctypes.byref(cfg), T, _ptr(topk_ids), capacity, align, _ptr(counts),
+                                  _ptr(offsets), _ptr(slot_of), _ptr(token_of), _ptr(err_flag), max_ctas,
+                                  _stream(stream)), "moe_plan_noalloc")
 
 
 def moe_dispatch(cfg, T, x, slot_of, xe, xe_scale=None, max_ctas=0, stream=None):
