@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--workload", default="qwen3_decode", choices=sorted(W.ALL))
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--routing", default=None, choices=[None, "uniform", "zipf"])
+    ap.add_argument("--capacity", type=int, default=None,
+                    help="rows per expert per ubatch (worst-token layout); -1 = the ubatch size")
     ap.add_argument("--comm-sms", type=int, default=COMM_SMS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the DBO-gain and e2e legs")
@@ -61,6 +63,8 @@ def workload(args):
         wl = wl.with_(T=args.T)
     if args.routing:
         wl = wl.with_(routing=args.routing)
+    if args.capacity is not None:
+        wl = wl.with_(capacity=wl.split if args.capacity < 0 else args.capacity)
     return wl
 
 

@@ -41,8 +41,10 @@ constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;  // full, empty, tmem full, tmem empty, drain
-constexpr size_t kSmemBytes =
-    1024 + (size_t)kStages * kStageBytes + kNumBars * 8 + 16 + 3 * (kMaxExperts + 1) * sizeof(int);
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kNumBars * 8 + 16 +
+                              3 * (kMaxExperts + 1) * sizeof(int) + 512 * sizeof(float) + 256 * sizeof(int);
+constexpr int kF8Threads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 promotion + epilogue
+constexpr int kF8BK = 128;       // e4m3 elements per k-block = one 128-wide scale block
 
 struct TcParams {
     CUtensorMap tmA;  // activations [max_rows][K] bf16
@@ -57,6 +59,9 @@ struct TcParams {
     void* out;
     int32_t* err;
     int reverse;
+    const float* a_scale;  // fp8: [max_rows][K/128] row-group scales of A
+    const float* b_scale;  // fp8: [NE][NB/128][K/128] block scales of B
+    float* out_scale;      // fp8 up: [max_rows][I/128] scales of the quantised h
 };
 
 struct Smem {
@@ -71,6 +76,8 @@ struct Smem {
     int* tstart;
     int* cnt;
     int* off;
+    float* xval;         // fp8 up epilogue: [2 parities][2 halves][128 rows] partial amax
+    volatile int* xseq;  // [2 halves][128 rows] tile sequence number of the value
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
@@ -88,6 +95,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     s.tstart = reinterpret_cast<int*>(s.tmem_base + 4);
     s.cnt = s.tstart + (kMaxExperts + 1);
     s.off = s.cnt + (kMaxExperts + 1);
+    s.xval = reinterpret_cast<float*>(s.off + (kMaxExperts + 1));
+    s.xseq = reinterpret_cast<volatile int*>(s.xval + 512);
     return s;
 }
 
@@ -159,7 +168,8 @@ __device__ void scan_tiles(const TcParams& p, const Smem& s) {
     if (lane == 31) s.tstart[p.NE] = incl;
 }
 
-template <bool kUp>
+// kKElems: elements per k-block (one 128-byte swizzle row): 64 bf16 or 128 e4m3.
+template <bool kUp, int kKElems>
 __device__ void producer(const TcParams& p, const Smem& s, int total) {
     int stage = 0;
     uint32_t phase = 0;
@@ -183,9 +193,9 @@ __device__ void producer(const TcParams& p, const Smem& s, int total) {
             uint8_t* a = s.stages + (size_t)stage * kStageBytes;
             uint8_t* b = a + kABytes;
             tc::mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
-            tc::tma_load_2d(a, &p.tmA, &s.full[stage], kb * kBK, t.row0);
-            tc::tma_load_2d(b, &p.tmB, &s.full[stage], kb * kBK, b0);
-            tc::tma_load_2d(b + kBBytes / 2, &p.tmB, &s.full[stage], kb * kBK, b1);
+            tc::tma_load_2d(a, &p.tmA, &s.full[stage], kb * kKElems, t.row0);
+            tc::tma_load_2d(b, &p.tmB, &s.full[stage], kb * kKElems, b0);
+            tc::tma_load_2d(b + kBBytes / 2, &p.tmB, &s.full[stage], kb * kKElems, b1);
             pending |= 1u << stage;
             pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {
@@ -350,11 +360,218 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_c
     const int total = s.tstart[p.NE];
 
     if (warp == 0) {
-        if (lane == 0) producer<kUp>(p, s, total);
+        if (lane == 0) producer<kUp, kBK>(p, s, total);
     } else if (warp == 1) {
         if (lane == 0) mma_issuer(p, s, total, tmem_base);
     } else {
         epilogue<kUp>(p, s, total, tmem_base);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- FP8 (e4m3) kernels
+//
+// Same tiles and TMA ring as the bf16 kernels, with k-blocks of 128 e4m3 elements (one
+// 128-byte row), which is exactly one 128-wide scale block.  Each k-block's four
+// kind::f8f6f4 MMAs (K = 32) write a fresh partial product into one of two TMEM
+// buffers; eight promotion warps read it back, multiply by a_scale[row][kb] *
+// b_scale[n-block][kb] (both powers of two) and accumulate in fp32 registers (each
+// thread: one row, 128 of the 256 columns), while the MMAs of the next k-block fill
+// the other buffer.  The up kernel's epilogue forms h = silu(g) * u, finds the 1x128
+// group amax of its row with its partner thread (the other half of the columns)
+// through shared memory, and stores h as e4m3 with its power-of-two scale; the down
+// kernel stores ye as bf16.
+
+__device__ void mma_issuer_f8(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
+    int stage = 0;
+    uint32_t phase = 0;
+    int pb = 0;
+    uint32_t pph = 0;
+    bool ok = true;
+    constexpr uint32_t idesc = tc::idesc_e4m3_f32(kBM, kBN);
+    for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (!tc::mbar_wait(&s.tempty[pb], pph ^ 1u, s.abort) || !tc::mbar_wait(&s.full[stage], phase, s.abort)) {
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)(pb * kBN);
+            const uint32_t a_addr = tc::smem_u32(s.stages + (size_t)stage * kStageBytes);
+            const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+            for (int kk = 0; kk < kF8BK / 32; ++kk)
+                tc::mma_e4m3(d, tc::desc_sw128_kmajor(a_addr + kk * 32), tc::desc_sw128_kmajor(b_addr + kk * 32),
+                             idesc, kk != 0 ? 1u : 0u);
+            tc::mma_commit(&s.empty[stage]);
+            tc::mma_commit(&s.tfull[pb]);
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            pb ^= 1;
+            if (pb == 0) pph ^= 1u;
+        }
+    }
+    if (!ok) fail(s, p.err);
+    tc::mma_commit(s.drain);
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(s.drain, 0) && tc::globaltimer() - t0 < tc::kWaitTimeoutNs) {
+    }
+}
+
+// acc[i] += partial[c0 + i] * sc for 32 columns of this thread's TMEM lane
+__device__ __forceinline__ void promote32(uint32_t taddr, float sc, float* acc) {
+    uint32_t v[32];
+    tc::tmem_ld32(taddr, v);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = fmaf(__uint_as_float(v[i]), sc, acc[i]);
+}
+
+template <bool kUp>
+__device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;           // TMEM lane quarter
+    const int half = (warp - 2) >> 2;  // which half of the 256 columns
+    const int r = q * 32 + lane;
+    const int ksb = p.K / kF8BK;      // scale blocks along K
+    int pb = 0;
+    uint32_t pph = 0;
+    int seq = 0;
+    bool ok = true;
+    for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
+        const Tile t = decode_tile(p, s, total, lin);
+        const int64_t row = (int64_t)t.row0 + r;
+        const bool in_rows = row < p.max_rows;
+        const float* asc = p.a_scale + (in_rows ? row : 0) * ksb;
+        const float* bsc = p.b_scale + (size_t)t.e * (p.NB / kF8BK) * ksb;
+        const int nb0 = kUp ? t.nt : 2 * t.nt + half;  // gate (up kernel) or output block
+        const int nb1 = kUp ? p.I / kF8BK + t.nt : nb0;  // up block (up kernel)
+        float acc[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (!tc::mbar_wait(&s.tfull[pb], pph, s.abort)) {
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            const float sa = in_rows ? __ldg(asc + kb) : 0.0f;
+            const float s0 = sa * __ldg(bsc + (size_t)nb0 * ksb + kb);
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(pb * kBN);
+            if (kUp) {
+                const float s1 = sa * __ldg(bsc + (size_t)nb1 * ksb + kb);
+                promote32(tb + 64 * half, s0, acc);
+                promote32(tb + 64 * half + 32, s0, acc + 32);
+                promote32(tb + 128 + 64 * half, s1, acc + 64);
+                promote32(tb + 128 + 64 * half + 32, s1, acc + 96);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) promote32(tb + 128 * half + 32 * c, s0, acc + 32 * c);
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&s.tempty[pb]);
+            pb ^= 1;
+            if (pb == 0) pph ^= 1u;
+        }
+        if (!ok) break;
+        const bool valid = r < t.rows;
+        if (kUp) {
+            // h for this thread's 64 columns (gate in acc[0..63], up in acc[64..127])
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const float g = acc[i];
+                acc[i] = g / (1.0f + expf(-g)) * acc[64 + i];
+                amax = fmaxf(amax, fabsf(acc[i]));
+            }
+            // the row's other 64 columns belong to the partner thread: exchange amax
+            ++seq;
+            const int par = seq & 1;
+            s.xval[(par * 2 + half) * 128 + r] = amax;
+            __threadfence_block();
+            s.xseq[half * 128 + r] = seq;
+            const uint64_t t0 = tc::globaltimer();
+            while (s.xseq[(1 - half) * 128 + r] < seq) {
+                if (*s.abort || tc::globaltimer() - t0 > tc::kWaitTimeoutNs) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) break;
+            __threadfence_block();
+            amax = fmaxf(amax, s.xval[(par * 2 + 1 - half) * 128 + r]);
+            const int se = fp8_scale_exp(amax);
+            if (valid) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint16_t lo = f2_to_e4m3x2(scalbnf(acc[4 * i], -se), scalbnf(acc[4 * i + 1], -se));
+                    const uint16_t hi = f2_to_e4m3x2(scalbnf(acc[4 * i + 2], -se), scalbnf(acc[4 * i + 3], -se));
+                    w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + row * p.I + t.nt * 128 + 64 * half);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                if (half == 0) p.out_scale[row * (p.I / kF8BK) + t.nt] = scalbnf(1.0f, se);
+            }
+        } else if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.H + t.nt * kBN + 128 * half);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                dst[i] = make_uint4(pack_bf16x2(acc[8 * i], acc[8 * i + 1]), pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
+                                    pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]),
+                                    pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
+        }
+    }
+    if (!ok) fail(s, p.err);
+}
+
+template <bool kUp>
+__global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem s = carve(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            tc::mbar_init(&s.full[i], 1);
+            tc::mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&s.tfull[i], 1);
+            tc::mbar_init(&s.tempty[i], 8);
+        }
+        tc::mbar_init(s.drain, 1);
+        *s.abort = 0;
+        tc::fence_barrier_init();
+        tc::prefetch_tmap(&p.tmA);
+        tc::prefetch_tmap(&p.tmB);
+    }
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) s.xseq[i] = 0;
+    if (warp == 1) {
+        tc::tmem_alloc(s.tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (warp == 2) scan_tiles(p, s);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem_base = *s.tmem_base;
+    const int total = s.tstart[p.NE];
+
+    if (warp == 0) {
+        if (lane == 0) producer<kUp, kF8BK>(p, s, total);
+    } else if (warp == 1) {
+        if (lane == 0) mma_issuer_f8(p, s, total, tmem_base);
+    } else {
+        epilogue_f8<kUp>(p, s, total, tmem_base);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -378,30 +595,32 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D K-major bf16 matrix [rows][inner], box 64 x 128 with the 128-byte swizzle.
-bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
+// 2-D K-major matrix [rows][inner] with the 128-byte swizzle and a box of one
+// 128-byte row (64 bf16 or 128 e4m3) by 128 rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, bool fp8) {
     auto enc = encode_fn();
     if (!enc) return false;
+    const uint64_t elt = fp8 ? 1 : 2;
     cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, 128};
+    cuuint64_t strides[1] = {inner * elt};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), 128};
     cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kUp>
+template <bool kUp, bool kFp8>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
     static int configured_dev = -1;
     const int dev = device_info().device;
+    auto kern = kFp8 ? ffn_tc_fp8_kernel<kUp> : ffn_tc_bf16_kernel<kUp>;
     if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_tc_bf16_kernel<kUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    ffn_tc_bf16_kernel<kUp><<<grid, kThreads, kSmemBytes, st>>>(p);
+    kern<<<grid, kFp8 ? kF8Threads : kThreads, kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -409,26 +628,30 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
 
 bool ffn_tc_supported(const moe_config& c) {
     const DeviceInfo& d = device_info();
-    return c.dtype == MOE_BF16 && d.cc_major == 10 && c.hidden % kBN == 0 && c.inter % 128 == 0 &&
-           c.hidden % kBK == 0 && d.smem_optin >= kSmemBytes && encode_fn() != nullptr;
+    return (c.dtype == MOE_BF16 || c.dtype == MOE_FP8_E4M3) && d.cc_major == 10 && c.hidden % kBN == 0 &&
+           c.inter % 128 == 0 && d.smem_optin >= kSmemBytes && encode_fn() != nullptr;
 }
 
 cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st) {
     const int NE = c.num_experts + c.num_shared;
     const int H = c.hidden, I = c.inter;
+    const bool fp8 = c.dtype == MOE_FP8_E4M3;
     int grid = device_info().num_sms;
     if (grid > grid_cap) grid = grid_cap;
     if (grid < 1) grid = 1;
     void* h = a.ws;
+    float* h_scale =
+        fp8 ? reinterpret_cast<float*>(static_cast<char*>(a.ws) + align_up((size_t)a.max_rows * I, 256)) : nullptr;
+    const int kelems = fp8 ? kF8BK : kBK;
     TcParams up{};
-    if (!make_map_bf16(&up.tmA, a.xe, (uint64_t)H, (uint64_t)a.max_rows) ||
-        !make_map_bf16(&up.tmB, a.w13, (uint64_t)H, (uint64_t)NE * 2 * I))
+    if (!make_map(&up.tmA, a.xe, (uint64_t)H, (uint64_t)a.max_rows, fp8) ||
+        !make_map(&up.tmB, a.w13, (uint64_t)H, (uint64_t)NE * 2 * I, fp8))
         return cudaErrorInvalidValue;
     up.counts = a.counts;
     up.offsets = a.offsets;
     up.NE = NE;
     up.K = H;
-    up.kblocks = H / kBK;
+    up.kblocks = H / kelems;
     up.NB = 2 * I;
     up.ntn = I / 128;
     up.I = I;
@@ -437,18 +660,24 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     up.out = h;
     up.err = a.err;
     up.reverse = a.reverse;
+    up.a_scale = a.xe_scale;
+    up.b_scale = a.w13_scale;
+    up.out_scale = h_scale;
     TcParams dn = up;
-    if (!make_map_bf16(&dn.tmA, h, (uint64_t)I, (uint64_t)a.max_rows) ||
-        !make_map_bf16(&dn.tmB, a.w2, (uint64_t)I, (uint64_t)NE * H))
+    if (!make_map(&dn.tmA, h, (uint64_t)I, (uint64_t)a.max_rows, fp8) ||
+        !make_map(&dn.tmB, a.w2, (uint64_t)I, (uint64_t)NE * H, fp8))
         return cudaErrorInvalidValue;
     dn.K = I;
-    dn.kblocks = I / kBK;
+    dn.kblocks = I / kelems;
     dn.NB = H;
     dn.ntn = H / kBN;
     dn.out = a.ye;
-    cudaError_t e = launch_one<true>(up, grid, st);
+    dn.a_scale = h_scale;
+    dn.b_scale = a.w2_scale;
+    dn.out_scale = nullptr;
+    cudaError_t e = fp8 ? launch_one<true, true>(up, grid, st) : launch_one<true, false>(up, grid, st);
     if (e != cudaSuccess) return e;
-    return launch_one<false>(dn, grid, st);
+    return fp8 ? launch_one<false, true>(dn, grid, st) : launch_one<false, false>(dn, grid, st);
 }
 
 }  // namespace moe
