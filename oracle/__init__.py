@@ -92,6 +92,12 @@ def lib():
             L.orc_max_rows.restype = ctypes.c_int64
             L.orc_moe_layer.argtypes = [P, i32, i32, P, P, P, P, P, P, P, P, P, i32, i32, P, P, P]
             L.orc_moe_layer.restype = i32
+            L.orc_combine_resid.argtypes = [P, i32, P, P, P, P, P]
+            L.orc_combine_resid.restype = None
+            L.orc_standin.argtypes = [P, i32, P, P, P]
+            L.orc_standin.restype = None
+            L.orc_moe_stack.argtypes = [P, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, i32, i32, P]
+            L.orc_moe_stack.restype = i32
             _lib = L
     return _lib
 
@@ -274,3 +280,54 @@ def moe_layer(cfg: Config, logits, x, weights, bias=None, split: int = 0, capaci
     st = lib().orc_moe_layer(ctypes.byref(c), T, split, _p(logits), _p(bias), _p(x),
                              *[_p(a) for a in args], capacity, align, _p(ids), _p(w), _p(y))
     return dict(status=int(st), ids=ids, w=w, y=y)
+
+
+def combine_resid(cfg: Config, ye, w, slot_of, resid):
+    """combine with a residual added before the single rounding."""
+    ye = _f32(ye)
+    w = _f64(w)
+    slot_of = _i32(slot_of)
+    resid = _f32(resid)
+    T = slot_of.shape[0]
+    y = np.zeros((T, cfg.hidden), np.float32)
+    c = cfg.c()
+    lib().orc_combine_resid(ctypes.byref(c), T, _p(ye), _p(w), _p(slot_of), _p(resid), _p(y))
+    return y
+
+
+def standin(cfg: Config, x, wa):
+    """a = x + x . Wa^T, rounded once (the stand-in for a layer's non-MoE compute)."""
+    x = _f32(x)
+    wa = _f32(wa)
+    a = np.zeros_like(x)
+    c = cfg.c()
+    lib().orc_standin(ctypes.byref(c), x.shape[0], _p(x), _p(wa), _p(a))
+    return a
+
+
+def moe_stack(cfg: Config, x0, layers, bias=None, split: int = 0, capacity: int = 0, align: int = 1):
+    """L layers; layers[l] = dict(wa=..., logits=..., and the weights as for moe_layer)."""
+    x0 = _f32(x0)
+    T = x0.shape[0]
+    L = len(layers)
+    keep = []
+
+    def arr(key, conv):
+        vals = [conv(ly.get(key)) for ly in layers]
+        keep.append(vals)
+        if all(v is None for v in vals):
+            return None
+        a = (ctypes.c_void_p * L)(*[None if v is None else v.ctypes.data for v in vals])
+        keep.append(a)
+        return a
+
+    wa = arr("wa", _f32)
+    lg = arr("logits", _f32)
+    ptrs = [arr("w13", _f32), arr("w13_q", _u8), arr("w13_s", _f32), arr("w2", _f32), arr("w2_q", _u8),
+            arr("w2_s", _f32)]
+    bias = _f32(bias)
+    out = np.zeros_like(x0)
+    c = cfg.c()
+    st = lib().orc_moe_stack(ctypes.byref(c), L, T, split, _p(x0), wa, lg, _p(bias), *ptrs, capacity, align,
+                             _p(out))
+    return dict(status=int(st), y=out)

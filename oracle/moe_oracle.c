@@ -499,12 +499,14 @@ void orc_expert_ffn(const orc_cfg* cfg, const int32_t* counts, const int32_t* of
 /* y[t] = sum_j w[t][j] * ye[slot_of[t][j]] + sum_s ye[slot_of[t][k+s]], summed in
  * double in (j, then s) order and rounded once to the output type.  Entries with
  * slot -1 contribute nothing. */
-void orc_combine(const orc_cfg* cfg, int32_t T, const float* ye, const double* w,
-                 const int32_t* slot_of, float* y) {
+/* The same with a residual: y[t] = resid[t] + sum ..., one rounding (resid may be
+ * NULL).  This is the combine of a layer inside a stack of layers. */
+void orc_combine_resid(const orc_cfg* cfg, int32_t T, const float* ye, const double* w,
+                       const int32_t* slot_of, const float* resid, float* y) {
     int32_t H = cfg->hidden, k = cfg->top_k, kk = k + cfg->num_shared;
     double* acc = (double*)malloc(sizeof(double) * (size_t)H);
     for (int32_t t = 0; t < T; ++t) {
-        for (int32_t n = 0; n < H; ++n) acc[n] = 0.0;
+        for (int32_t n = 0; n < H; ++n) acc[n] = resid ? (double)resid[(size_t)t * H + n] : 0.0;
         for (int32_t j = 0; j < kk; ++j) {
             int32_t r = slot_of[(size_t)t * kk + j];
             if (r < 0) continue;
@@ -514,6 +516,11 @@ void orc_combine(const orc_cfg* cfg, int32_t T, const float* ye, const double* w
         for (int32_t n = 0; n < H; ++n) y[(size_t)t * H + n] = round_out(cfg->dtype, acc[n]);
     }
     free(acc);
+}
+
+void orc_combine(const orc_cfg* cfg, int32_t T, const float* ye, const double* w,
+                 const int32_t* slot_of, float* y) {
+    orc_combine_resid(cfg, T, ye, w, slot_of, NULL, y);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -570,7 +577,7 @@ int64_t orc_max_rows(const orc_cfg* cfg, int32_t T, int32_t capacity, int32_t al
 /* route -> plan -> dispatch -> FFN -> combine on tokens [t0, t0 + T). */
 static int32_t layer_range(const orc_cfg* cfg, int32_t t0, int32_t T, const float* logits,
                            const float* bias, const float* x, const orc_weights* W, int32_t capacity,
-                           int32_t align, int32_t* ids, double* w, float* y) {
+                           int32_t align, int32_t* ids, double* w, const float* resid, float* y) {
     int32_t H = cfg->hidden, k = cfg->top_k, E = cfg->num_experts, S = cfg->num_shared;
     int32_t NE = E + S, kk = k + S;
     int32_t cap = capacity;
@@ -594,7 +601,8 @@ static int32_t layer_range(const orc_cfg* cfg, int32_t t0, int32_t T, const floa
     orc_dispatch(cfg, T, x + (size_t)t0 * H, slot_of, xe, xe_q, xe_s);
     orc_expert_ffn(cfg, counts, offsets, xe, xe_q, xe_s, W->w13, W->w13_q, W->w13_s, W->w2, W->w2_q,
                    W->w2_s, ye);
-    orc_combine(cfg, T, ye, w + (size_t)t0 * k, slot_of, y + (size_t)t0 * H);
+    orc_combine_resid(cfg, T, ye, w + (size_t)t0 * k, slot_of, resid ? resid + (size_t)t0 * H : NULL,
+                      y + (size_t)t0 * H);
     free(counts);
     free(offsets);
     free(slot_of);
@@ -617,8 +625,66 @@ int32_t orc_moe_layer(const orc_cfg* cfg, int32_t T, int32_t split, const float*
                       int32_t capacity, int32_t align, int32_t* ids, double* w, float* y) {
     orc_weights W = {w13, w13_q, w13_s, w2, w2_q, w2_s};
     if (split <= 0 || split >= T)
-        return layer_range(cfg, 0, T, logits, bias, x, &W, capacity, align, ids, w, y);
-    int32_t s0 = layer_range(cfg, 0, split, logits, bias, x, &W, capacity, align, ids, w, y);
-    int32_t s1 = layer_range(cfg, split, T - split, logits, bias, x, &W, capacity, align, ids, w, y);
+        return layer_range(cfg, 0, T, logits, bias, x, &W, capacity, align, ids, w, NULL, y);
+    int32_t s0 = layer_range(cfg, 0, split, logits, bias, x, &W, capacity, align, ids, w, NULL, y);
+    int32_t s1 = layer_range(cfg, split, T - split, logits, bias, x, &W, capacity, align, ids, w, NULL, y);
     return s0 != ORC_OK ? s0 : s1;
+}
+
+/* ------------------------------------------------------------------------- */
+/* A stack of layers                                                         */
+/* ------------------------------------------------------------------------- */
+
+/* The stand-in for a layer's non-MoE compute (reading: the pages overlap dispatch
+ * and combine with "the other microbatch's non-MoE compute" -- attention and the
+ * like -- whose content is outside this library; a dense projection with a residual
+ * stands in for it):  a[t] = x[t] + x[t] . Wa^T,  Wa [H][H] K-major, summed in
+ * double, rounded once to the activation storage type. */
+void orc_standin(const orc_cfg* cfg, int32_t T, const float* x, const float* wa, float* a) {
+    int32_t H = cfg->hidden;
+    for (int32_t t = 0; t < T; ++t)
+        for (int32_t n = 0; n < H; ++n) {
+            double acc = 0.0;
+            for (int32_t kx = 0; kx < H; ++kx) acc += (double)x[(size_t)t * H + kx] * (double)wa[(size_t)n * H + kx];
+            a[(size_t)t * H + n] = round_out(cfg->dtype, (double)x[(size_t)t * H + n] + acc);
+        }
+}
+
+/* L layers; layer l:  a = x_l + x_l . Wa_l^T (stand-in),  x_{l+1} = a + MoE_l(a), the
+ * MoE part routed by the given logits_l and combined onto the residual a with one
+ * rounding.  Weights / logits of layer l are at the given per-layer pointers.  Each
+ * layer runs as two micro-batches when split > 0, like the layer above. */
+int32_t orc_moe_stack(const orc_cfg* cfg, int32_t L, int32_t T, int32_t split, const float* x0,
+                      const float* const* wa, const float* const* logits, const float* bias,
+                      const float* const* w13, const uint8_t* const* w13_q, const float* const* w13_s,
+                      const float* const* w2, const uint8_t* const* w2_q, const float* const* w2_s,
+                      int32_t capacity, int32_t align, float* out) {
+    int32_t H = cfg->hidden, k = cfg->top_k;
+    size_t n = (size_t)T * H;
+    float* x = (float*)malloc(sizeof(float) * n);
+    float* a = (float*)malloc(sizeof(float) * n);
+    int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
+    double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
+    int32_t st = ORC_OK;
+    memcpy(x, x0, sizeof(float) * n);
+    for (int32_t l = 0; l < L; ++l) {
+        orc_weights W = {w13 ? w13[l] : NULL, w13_q ? w13_q[l] : NULL, w13_s ? w13_s[l] : NULL,
+                         w2 ? w2[l] : NULL,   w2_q ? w2_q[l] : NULL,   w2_s ? w2_s[l] : NULL};
+        orc_standin(cfg, T, x, wa[l], a);
+        int32_t r;
+        if (split <= 0 || split >= T) {
+            r = layer_range(cfg, 0, T, logits[l], bias, a, &W, capacity, align, ids, w, a, x);
+        } else {
+            r = layer_range(cfg, 0, split, logits[l], bias, a, &W, capacity, align, ids, w, a, x);
+            int32_t r1 = layer_range(cfg, split, T - split, logits[l], bias, a, &W, capacity, align, ids, w, a, x);
+            if (r == ORC_OK) r = r1;
+        }
+        if (st == ORC_OK) st = r;
+    }
+    memcpy(out, x, sizeof(float) * n);
+    free(x);
+    free(a);
+    free(ids);
+    free(w);
+    return st;
 }
