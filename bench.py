@@ -154,9 +154,11 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """The slowest rank's time (every rank gets it)."""
     if world == 1:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 
