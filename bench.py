@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--comm-sms", type=int, default=COMM_SMS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the DBO-gain and e2e legs")
+    ap.add_argument("--stack", type=int, default=0,
+                    help="time a stack of this many layers (stand-in block + MoE layer each) instead of one layer")
     return ap.parse_args()
 
 
@@ -317,6 +319,82 @@ def run_ours(args, rank, world, local):
     return out, wl
 
 
+def run_stack(args, rank, world, local):
+    """A stack of L layers (moe_stack_dbo): tokens/s through all layers, with the events
+    recorded before the yield (the fix) and after it (the old placement), and unsplit."""
+    from moe_expert_dispatch_route_gb300 import binding as B
+    from moe_expert_dispatch_route_gb300 import synth
+
+    wl = workload(args)
+    L = args.stack
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = B.config_of(wl)
+    T = wl.T
+    layers = []
+    for l in range(L):
+        g = torch.Generator(device=dev)
+        g.manual_seed(9000 + l)
+        ly = dict(logits=synth.logits(T, wl.num_experts, wl.routing, wl.seed + 10 * l, dev),
+                  wa=(torch.randn(wl.hidden, wl.hidden, generator=g, device=dev) * 0.01).to(torch.bfloat16))
+        ly.update(synth.weights(wl.num_experts + wl.num_shared, wl.hidden, wl.inter, wl.dtype, wl.w_std,
+                                wl.seed + 10 * l, dev))
+        layers.append(ly)
+    x = synth.hidden(T, wl.hidden, "bf16", 1.0, wl.seed, dev)
+    out = torch.zeros_like(x)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(B.moe_stack_workspace_size(cfg, T, wl.capacity, wl.align), dtype=torch.uint8, device=dev)
+    sa = B.StackArgs(x, out, layers, ws, None, err)
+    h = B.moe_dbo_create()
+    comm = torch.cuda.Stream(device=dev)
+    compute = torch.cuda.Stream(device=dev)
+
+    def graph(split, before):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(compute):
+            B.moe_stack_dbo(h, cfg, sa, T, split, 4, wl.capacity, wl.align, args.comm_sms, before, compute, comm)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=compute):
+                B.moe_stack_dbo(h, cfg, sa, T, split, 4, wl.capacity, wl.align, args.comm_sms, before, compute, comm)
+        torch.cuda.synchronize()
+        return g
+
+    def timed(g, sample=False):
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        sampler = ClockSampler(local) if sample else None
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(compute):
+            e0.record(compute)
+            for _ in range(args.steps):
+                g.replay()
+            e1.record(compute)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1) / args.steps, world), (sampler.stop() if sampler else None)
+
+    ms_fix, clocks = timed(graph(0, 1), sample=True)
+    ms_old, _ = timed(graph(0, 0))
+    ms_unsplit, _ = timed(graph(T, 1))
+    assert int(err.item()) == 0
+    B.moe_dbo_destroy(h)
+    out = {"metric": f"MoE stack tokens/s ({L} layers of stand-in block + MoE layer, DBO) at 1 GB300",
+           "value": round(T * world / (ms_fix / 1e3), 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms_fix, 5), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "fp8e4m3"}[wl.dtype],
+           "data": "synthetic", "config": {"workload": wl.describe(), "layers": L, "comm_sms": args.comm_sms},
+           "clocks": clocks,
+           "stack": {"ms_event_before_yield": round(ms_fix, 5), "ms_event_after_yield": round(ms_old, 5),
+                     "gain_of_event_before_yield": round(ms_old / ms_fix, 4),
+                     "ms_unsplit": round(ms_unsplit, 5), "gain_vs_unsplit": round(ms_unsplit / ms_fix, 4)}}
+    return out
+
+
 def weights_bytes(wl) -> float:
     NE = wl.num_experts + wl.num_shared
     elt = {"f32": 4, "bf16": 2, "fp8": 1}[wl.dtype]
@@ -509,6 +587,14 @@ def main():
         if out is not None:
             print(json.dumps(out), flush=True)
         if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    if args.stack > 0:
+        out = run_stack(args, rank, world, local)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        if world > 1:
+            torch.distributed.barrier()
             torch.distributed.destroy_process_group()
         return
     out, wl = run_ours(args, rank, world, local)

@@ -283,9 +283,49 @@ enum {
     MOE_OP_FFN = 3,
     MOE_OP_COMBINE = 4,
     MOE_OP_RECORD = 5,
-    MOE_OP_WAIT = 6
+    MOE_OP_WAIT = 6,
+    MOE_OP_STANDIN = 7
 };
 MOE_API int32_t moe_dbo_schedule(int32_t two_ubatches, int32_t* ops, int32_t max_ops);
+
+/* ---------------------------------------------------------------------------
+ * A stack of L layers with Dual-Batch Overlap across layer boundaries.  The pages'
+ * overlap is across a whole model step: one ubatch's dispatch and combine run under
+ * the other ubatch's non-MoE compute as well as its experts ([C] Purpose: combine of
+ * one ubatch overlapped with the other ubatch's non-MoE compute).  Layer l here is
+ *     a   = x_l + x_l . Wa_l^T            a stand-in for the non-MoE compute
+ *     x_{l+1} = a + MoE_l(a)              routed by the given logits_l,
+ * the stand-in a dense bf16 projection with a residual (one rounding), the MoE part
+ * as moe_layer_dbo with the residual added inside combine (one rounding).
+ * Compute stream: stand-in and experts; comm stream: route, plan, dispatch, combine.
+ * event_before_yield = 1 records each event a comm step waits on right after the
+ * compute kernel it stands for ([C] Purpose); 0 reproduces the placement before that
+ * fix (recorded after the other ubatch's compute was enqueued), for measurement.  Both
+ * give identical results.  Activations must be bf16 (MOE_BF16 / MOE_FP8_E4M3 layers)
+ * and hidden a multiple of 256, else MOE_ERR_UNSUPPORTED. */
+typedef struct {
+    const void* x;                      /* device [T][H] bf16: input of layer 0 */
+    void* out;                          /* device [T][H] bf16: output of layer L-1 */
+    const float* const* logits;         /* host array of L device pointers, each fp32 [T][E] */
+    const float* bias;                  /* device fp32 [E] or NULL, every layer */
+    const void* const* wa;              /* host array of L device pointers, each bf16 [H][H] (K-major) */
+    const void* const* w13;             /* host arrays of L device pointers, layouts as in */
+    const float* const* w13_scale;      /* moe_expert_ffn (scales: FP8 only, else NULL) */
+    const void* const* w2;
+    const float* const* w2_scale;
+    int32_t* err_flag;                  /* device int32 or NULL (workspace flag); reset by the call */
+    void* workspace;                    /* moe_stack_workspace_size bytes, 256-byte aligned */
+    size_t workspace_bytes;
+} moe_stack_args;
+
+MOE_API size_t moe_stack_workspace_size(const moe_config* cfg, int32_t T, int32_t capacity, int32_t align);
+MOE_API moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_stack_args* args,
+                                 int32_t L, int32_t T, int32_t split, int32_t min_tokens, int32_t capacity,
+                                 int32_t align, int32_t comm_sms, int32_t event_before_yield,
+                                 moe_stream_t compute, moe_stream_t comm);
+/* The stack's enqueue schedule (same record format as moe_dbo_schedule; layer by layer). */
+MOE_API int32_t moe_stack_schedule(int32_t layers, int32_t two_ubatches, int32_t event_before_yield,
+                                   int32_t* ops, int32_t max_ops);
 
 MOE_API const char* moe_status_string(moe_status s);
 

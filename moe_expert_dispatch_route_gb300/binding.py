@@ -20,7 +20,7 @@ GATE_SOFTMAX, GATE_SIGMOID_GROUPED = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_CAPACITY", 7: "MOE_ERR_BAD_INDEX",
           8: "MOE_ERR_TIMEOUT"}
-OPS = {0: "route", 1: "plan", 2: "dispatch", 3: "ffn", 4: "combine", 5: "record", 6: "wait"}
+OPS = {0: "route", 1: "plan", 2: "dispatch", 3: "ffn", 4: "combine", 5: "record", 6: "wait", 7: "standin"}
 
 
 class MoeError(RuntimeError):
@@ -36,6 +36,14 @@ class MoeConfig(ctypes.Structure):
                 ("renormalize", ctypes.c_int32), ("n_group", ctypes.c_int32),
                 ("topk_group", ctypes.c_int32), ("routed_scale", ctypes.c_float),
                 ("dtype", ctypes.c_int32)]
+
+
+class MoeStackArgs(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("out", ctypes.c_void_p), ("logits", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("wa", ctypes.c_void_p), ("w13", ctypes.c_void_p),
+                ("w13_scale", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
+                ("err_flag", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 class MoeLayerArgs(ctypes.Structure):
@@ -78,6 +86,10 @@ _SIGS = {
     "moe_layer_dbo": (_I32, [_P, _CFG, ctypes.POINTER(MoeLayerArgs), _I32, _I32, _I32, _I32, _I32, _I32,
                              _P, _P]),
     "moe_dbo_schedule": (_I32, [_I32, _P, _I32]),
+    "moe_stack_workspace_size": (_SZ, [_CFG, _I32, _I32, _I32]),
+    "moe_stack_dbo": (_I32, [_P, _CFG, ctypes.POINTER(MoeStackArgs), _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                             _I32, _P, _P]),
+    "moe_stack_schedule": (_I32, [_I32, _I32, _I32, _P, _I32]),
     "moe_status_string": (ctypes.c_char_p, [_I32]),
 }
 EXPORTS = tuple(_SIGS)
@@ -220,3 +232,43 @@ def layer_args(logits, x, weights: dict, y, topk_ids, topk_w, workspace, bias=No
     return MoeLayerArgs(_ptr(logits), _ptr(bias), _ptr(x), _ptr(w13), _ptr(weights.get("w13_s")), _ptr(w2),
                         _ptr(weights.get("w2_s")), _ptr(y), _ptr(topk_ids), _ptr(topk_w), _ptr(err_flag),
                         _ptr(workspace), workspace.numel() * workspace.element_size())
+
+
+def moe_stack_workspace_size(cfg, T, capacity=0, align=128) -> int:
+    return int(lib().moe_stack_workspace_size(ctypes.byref(cfg), T, capacity, align))
+
+
+class StackArgs:
+    """moe_stack_args from tensors; keeps the host pointer arrays alive.
+    layers: list of dicts with "logits", "wa" and the weights ({"w13","w2"} or fp8 keys)."""
+
+    def __init__(self, x, out, layers, workspace, bias=None, err_flag=None):
+        L = len(layers)
+        arr = lambda vals: (ctypes.c_void_p * L)(*[_ptr(v) for v in vals])
+        self._keep = [arr([ly["logits"] for ly in layers]), arr([ly["wa"] for ly in layers]),
+                      arr([ly.get("w13", ly.get("w13_q")) for ly in layers]),
+                      arr([ly.get("w13_s") for ly in layers]),
+                      arr([ly.get("w2", ly.get("w2_q")) for ly in layers]),
+                      arr([ly.get("w2_s") for ly in layers])]
+        lg, wa, w13, w13s, w2, w2s = self._keep
+        self.c = MoeStackArgs(_ptr(x), _ptr(out), ctypes.cast(lg, ctypes.c_void_p), _ptr(bias),
+                              ctypes.cast(wa, ctypes.c_void_p), ctypes.cast(w13, ctypes.c_void_p),
+                              ctypes.cast(w13s, ctypes.c_void_p), ctypes.cast(w2, ctypes.c_void_p),
+                              ctypes.cast(w2s, ctypes.c_void_p), _ptr(err_flag), _ptr(workspace),
+                              workspace.numel() * workspace.element_size())
+        self.L = L
+
+
+def moe_stack_dbo(handle, cfg, args: StackArgs, T, split=0, min_tokens=4, capacity=0, align=128, comm_sms=0,
+                  event_before_yield=1, compute=None, comm=None):
+    cs = _stream(compute)
+    ms = _stream(comm) if comm is not None else cs
+    _check(lib().moe_stack_dbo(handle, ctypes.byref(cfg), ctypes.byref(args.c), args.L, T, split, min_tokens,
+                               capacity, align, comm_sms, int(event_before_yield), cs, ms), "moe_stack_dbo")
+
+
+def moe_stack_schedule(layers: int, two_ubatches: bool = True, event_before_yield: bool = True):
+    n = lib().moe_stack_schedule(layers, int(two_ubatches), int(event_before_yield), None, 0)
+    buf = (ctypes.c_int32 * (4 * n))()
+    lib().moe_stack_schedule(layers, int(two_ubatches), int(event_before_yield), buf, n)
+    return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]

@@ -12,7 +12,8 @@ constexpr int kCombineThreads = 256;
 template <bool kF32>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     int T, int k, int kk, int nvec, const uint4* __restrict__ ye, const float* __restrict__ w,
-    const int32_t* __restrict__ slot_of, uint4* __restrict__ y) {
+    const int32_t* __restrict__ slot_of, uint4* __restrict__ y, const uint4* __restrict__ resid) {
+    pdl_begin();
     constexpr int kPer = kF32 ? 4 : 8;  // elements per 16-byte vector
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -23,19 +24,33 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
             float acc[kPer];
 #pragma unroll
             for (int i = 0; i < kPer; ++i) acc[i] = 0.0f;
-            int j = 0;
-            for (; j + 4 <= kk; j += 4) {
-                uint4 val[4];
-                int r[4];
-                float wj[4];
+            if (resid) {  // the residual starts the sum (one rounding at the end)
+                const uint4 rv = __ldg(resid + (size_t)t * nvec + v);
+                const uint32_t rd[4] = {rv.x, rv.y, rv.z, rv.w};
+                if (kF32) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                    for (int i = 0; i < 4; ++i) acc[i] = __uint_as_float(rd[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[2 * i] = bf16_bits_to_f((uint16_t)(rd[i] & 0xffffu));
+                        acc[2 * i + 1] = bf16_bits_to_f((uint16_t)(rd[i] >> 16));
+                    }
+                }
+            }
+            int j = 0;
+            for (; j + 8 <= kk; j += 8) {  // eight row loads in flight per lane
+                uint4 val[8];
+                int r[8];
+                float wj[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
                     r[u] = __shfl_sync(0xffffffffu, my_slot, j + u);
                     wj[u] = __shfl_sync(0xffffffffu, my_w, j + u);
                     if (r[u] >= 0) val[u] = __ldg(ye + (size_t)r[u] * nvec + v);
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < 8; ++u) {
                     if (r[u] < 0) continue;
                     const uint32_t wd[4] = {val[u].x, val[u].y, val[u].z, val[u].w};
                     if (kF32) {
@@ -81,19 +96,19 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
 }
 
 cudaError_t launch_combine(const moe_config& c, int T, const void* ye, const float* w,
-                           const int32_t* slot_of, void* y, int grid_cap, cudaStream_t st) {
+                           const int32_t* slot_of, void* y, int grid_cap, cudaStream_t st, const void* resid) {
     if (T <= 0) return cudaSuccess;
     const int kk = c.top_k + c.num_shared;
     const int nvec = c.hidden * io_bytes(c.dtype) / 16;
     int grid = (T + 7) / 8;
     if (grid > grid_cap) grid = grid_cap;
     if (c.dtype == MOE_F32)
-        combine_kernel<true><<<grid, kCombineThreads, 0, st>>>(T, c.top_k, kk, nvec, static_cast<const uint4*>(ye), w,
-                                                              slot_of, static_cast<uint4*>(y));
-    else
-        combine_kernel<false><<<grid, kCombineThreads, 0, st>>>(T, c.top_k, kk, nvec, static_cast<const uint4*>(ye), w,
-                                                               slot_of, static_cast<uint4*>(y));
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<true>, grid, kCombineThreads, 0, st, T, c.top_k, kk, nvec,
+                          static_cast<const uint4*>(ye), w, slot_of, static_cast<uint4*>(y),
+                          static_cast<const uint4*>(resid));
+    return launch_pdl(combine_kernel<false>, grid, kCombineThreads, 0, st, T, c.top_k, kk, nvec,
+                      static_cast<const uint4*>(ye), w, slot_of, static_cast<uint4*>(y),
+                      static_cast<const uint4*>(resid));
 }
 
 }  // namespace moe

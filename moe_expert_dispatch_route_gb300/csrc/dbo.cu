@@ -28,7 +28,9 @@
 namespace moe {
 namespace {
 
-enum { kEvStart = 0, kEvDisp0, kEvFfn0, kEvDisp1, kEvFfn1, kEvDone, kNumEvents };
+enum { kEvStart = 0, kEvDisp0, kEvFfn0, kEvDisp1, kEvFfn1, kEvDone,
+       // stack of layers: stand-in done, dispatch done, FFN done, combine done, per ubatch
+       kSevA0, kSevA1, kSevD0, kSevD1, kSevF0, kSevF1, kSevC0, kSevC1, kNumEvents };
 
 struct Op {
     int stream;  // 0 compute, 1 comm
@@ -70,6 +72,64 @@ std::vector<Op> make_schedule(bool two) {
     add(1, MOE_OP_COMBINE, 1, -1);
     add(1, MOE_OP_RECORD, -1, kEvDone);
     add(0, MOE_OP_WAIT, -1, kEvDone);     // join: nothing of the layer stays on the comm stream
+    return s;
+}
+
+// A stack of layers, each = stand-in non-MoE block (A) then the MoE layer: dispatch
+// side D (route, plan, dispatch), experts F, combine C.  Compute stream: A0 A1 F0 F1 per
+// layer; comm stream: D0 D1 C0 C1.  D(u) waits for A(u), F(u) for D(u), C(u) for F(u),
+// A(u) of the next layer for C(u).  With event_before_yield the event a comm step
+// waits on is recorded right after the compute kernel it stands for, so D0 overlaps A1,
+// D1 overlaps F0, C0 overlaps F1 and C1 overlaps the next layer's A0.  Without it (the
+// placement before "[Perf] Fix DBO overlap: capture DeepEP event before yield") the
+// event is recorded only after the other ubatch's compute has been enqueued too, so
+// D0 also waits for A1 and C0 for F1.
+std::vector<Op> make_stack_schedule(int L, bool two, bool before_yield) {
+    std::vector<Op> s;
+    auto add = [&](int st, int op, int ub, int ev) { s.push_back(Op{st, op, ub, ev}); };
+    if (!two) {
+        for (int l = 0; l < L; ++l) {
+            add(0, MOE_OP_STANDIN, 0, -1);
+            add(0, MOE_OP_ROUTE, 0, -1);
+            add(0, MOE_OP_PLAN, 0, -1);
+            add(0, MOE_OP_DISPATCH, 0, -1);
+            add(0, MOE_OP_FFN, 0, -1);
+            add(0, MOE_OP_COMBINE, 0, -1);
+        }
+        return s;
+    }
+    add(0, MOE_OP_RECORD, -1, kEvStart);
+    add(1, MOE_OP_WAIT, -1, kEvStart);
+    for (int l = 0; l < L; ++l) {
+        if (l > 0) add(0, MOE_OP_WAIT, 0, kSevC0);
+        add(0, MOE_OP_STANDIN, 0, -1);
+        if (before_yield) add(0, MOE_OP_RECORD, 0, kSevA0);
+        if (l > 0) add(0, MOE_OP_WAIT, 1, kSevC1);
+        add(0, MOE_OP_STANDIN, 1, -1);
+        if (!before_yield) add(0, MOE_OP_RECORD, 0, kSevA0);
+        add(0, MOE_OP_RECORD, 1, kSevA1);
+        for (int u = 0; u < 2; ++u) {
+            add(1, MOE_OP_WAIT, u, u ? kSevA1 : kSevA0);
+            add(1, MOE_OP_ROUTE, u, -1);
+            add(1, MOE_OP_PLAN, u, -1);
+            add(1, MOE_OP_DISPATCH, u, -1);
+            add(1, MOE_OP_RECORD, u, u ? kSevD1 : kSevD0);
+        }
+        add(0, MOE_OP_WAIT, 0, kSevD0);
+        add(0, MOE_OP_FFN, 0, -1);
+        if (before_yield) add(0, MOE_OP_RECORD, 0, kSevF0);
+        add(0, MOE_OP_WAIT, 1, kSevD1);
+        add(0, MOE_OP_FFN, 1, -1);
+        if (!before_yield) add(0, MOE_OP_RECORD, 0, kSevF0);
+        add(0, MOE_OP_RECORD, 1, kSevF1);
+        for (int u = 0; u < 2; ++u) {
+            add(1, MOE_OP_WAIT, u, u ? kSevF1 : kSevF0);
+            add(1, MOE_OP_COMBINE, u, -1);
+            add(1, MOE_OP_RECORD, u, u ? kSevC1 : kSevC0);
+        }
+    }
+    add(1, MOE_OP_RECORD, -1, kEvDone);
+    add(0, MOE_OP_WAIT, -1, kEvDone);
     return s;
 }
 
@@ -209,7 +269,11 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
         float* xe_scale = c.dtype == MOE_FP8_E4M3 ? reinterpret_cast<float*>(b + L.xe_scale) : nullptr;
         void* ye = b + L.ye;
         const int Tu = tn[u];
-        const int comm_grid = two ? comm_cap : sms * 8;
+        // the SM budget applies to the comm-side steps that overlap an FFN (ubatch 1's
+        // route / plan / dispatch, ubatch 0's combine); ubatch 0's first steps and
+        // ubatch 1's combine run alone and get the whole GPU
+        const bool overlapped = (u == 1 && op.op != MOE_OP_COMBINE) || (u == 0 && op.op == MOE_OP_COMBINE);
+        const int comm_grid = (two && overlapped) ? comm_cap : sms * 8;
         const int ffn_grid = two ? ffn_cap : sms * 8;
         const float* logits_u = a->logits + (size_t)t0[u] * c.num_experts;
         int32_t* ids_u = a->topk_ids + (size_t)t0[u] * k;
@@ -245,6 +309,145 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
         }
     }
     return st;
+}
+
+
+int32_t moe_stack_schedule(int32_t layers, int32_t two_ubatches, int32_t event_before_yield, int32_t* ops,
+                           int32_t max_ops) {
+    if (layers < 1) return 0;
+    std::vector<Op> s = make_stack_schedule(layers, two_ubatches != 0, event_before_yield != 0);
+    if (ops)
+        for (int i = 0; i < (int)s.size() && i < max_ops; ++i) {
+            ops[4 * i + 0] = s[i].stream;
+            ops[4 * i + 1] = s[i].op;
+            ops[4 * i + 2] = s[i].ub;
+            ops[4 * i + 3] = s[i].ev;
+        }
+    return (int32_t)s.size();
+}
+
+namespace {
+struct StackLayout {
+    UbLayout ub;
+    size_t ub_base[2], a[2], ids[2], w[2], pp[2], total;
+};
+StackLayout stack_layout(const moe_config& c, int T, int capacity, int align) {
+    StackLayout S{};
+    S.ub = ub_layout(c, T, capacity, align);
+    const size_t act = align_up((size_t)T * c.hidden * io_bytes(c.dtype), 256);
+    const size_t ids = align_up((size_t)T * c.top_k * 4, 256);
+    size_t o = 256;  // error flag
+    for (int u = 0; u < 2; ++u) {
+        S.ub_base[u] = o;
+        o += S.ub.total;
+    }
+    for (int u = 0; u < 2; ++u) {
+        S.a[u] = o;
+        o += act;
+        S.ids[u] = o;
+        o += ids;
+        S.w[u] = o;
+        o += ids;
+        S.pp[u] = o;
+        o += act;
+    }
+    S.total = o;
+    return S;
+}
+}  // namespace
+
+size_t moe_stack_workspace_size(const moe_config* cfg, int32_t T, int32_t capacity, int32_t align) {
+    if (check_config(cfg) != MOE_OK || T < 0 || capacity < 0 || align < 1) return 0;
+    return stack_layout(*cfg, T, capacity, align).total;
+}
+
+moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_stack_args* a, int32_t L, int32_t T,
+                         int32_t split, int32_t min_tokens, int32_t capacity, int32_t align, int32_t comm_sms,
+                         int32_t event_before_yield, moe_stream_t compute_s, moe_stream_t comm_s) {
+    if (!h || !cfg || !a) return MOE_ERR_INVALID_ARG;
+    if (L < 1 || T < 0 || split < 0 || capacity < 0 || align < 1 || comm_sms < 0) return MOE_ERR_INVALID_ARG;
+    const moe_status cs_ok = check_config(cfg);
+    if (cs_ok != MOE_OK) return cs_ok;
+    if (!standin_tc_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!a->x || !a->out || !a->logits || !a->wa || !a->w13 || !a->w2) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = cfg->dtype == MOE_FP8_E4M3;
+    for (int l = 0; l < L; ++l) {
+        if (!a->logits[l] || !a->wa[l] || !a->w13[l] || !a->w2[l]) return MOE_ERR_INVALID_ARG;
+        if (fp8 && (!a->w13_scale || !a->w2_scale || !a->w13_scale[l] || !a->w2_scale[l])) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(a->wa[l]) || !aligned16(a->w13[l]) || !aligned16(a->w2[l])) return MOE_ERR_ALIGNMENT;
+    }
+    if (!aligned16(a->x) || !aligned16(a->out)) return MOE_ERR_ALIGNMENT;
+    if ((int64_t)moe_plan_rows(cfg, T, capacity, align) > (int64_t)INT32_MAX) return MOE_ERR_INVALID_ARG;
+    const StackLayout S = stack_layout(*cfg, T, capacity, align);
+    if (!a->workspace || a->workspace_bytes < S.total) return MOE_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return MOE_ERR_ALIGNMENT;
+
+    const moe_config& c = *cfg;
+    cudaStream_t cs = (cudaStream_t)compute_s, ms = (cudaStream_t)comm_s;
+    int s = split == 0 ? (T + 1) / 2 : split;
+    const bool two = T >= (min_tokens > 2 ? min_tokens : 2) && s > 0 && s < T;
+    if (!two) s = T;
+    const int t0[2] = {0, s};
+    const int tn[2] = {s, T - s};
+    const int sms = device_info().num_sms;
+    const int comm_cap = comm_sms > 0 ? comm_sms : sms * 8;
+    const int ffn_cap = comm_sms > 0 ? (sms - comm_sms > 1 ? sms - comm_sms : 1) : sms * 8;
+    char* ws = static_cast<char*>(a->workspace);
+    int32_t* err = a->err_flag ? a->err_flag : reinterpret_cast<int32_t*>(ws);
+    const UbLayout& U = S.ub;
+    const size_t H = c.hidden, rowb = H * io_bytes(c.dtype);
+    if (cudaMemsetAsync(err, 0, sizeof(int32_t), cs) != cudaSuccess) return MOE_ERR_CUDA;
+
+    int layer[2] = {-1, -1};  // current layer of each ubatch (advanced by its stand-in)
+    for (const Op& op : make_stack_schedule(L, two, event_before_yield != 0)) {
+        cudaStream_t q = op.stream == 0 ? cs : ms;
+        const int u = op.ub < 0 ? 0 : op.ub;
+        if (op.op == MOE_OP_STANDIN) ++layer[u];
+        const int l = layer[u] < 0 ? 0 : layer[u];
+        char* b = ws + S.ub_base[u];
+        int32_t* counts = reinterpret_cast<int32_t*>(b + U.counts);
+        int32_t* offsets = reinterpret_cast<int32_t*>(b + U.offsets);
+        int32_t* slot_of = reinterpret_cast<int32_t*>(b + U.slot_of);
+        int32_t* token_of = reinterpret_cast<int32_t*>(b + U.token_of);
+        void* xe = b + U.xe;
+        float* xe_scale = fp8 ? reinterpret_cast<float*>(b + U.xe_scale) : nullptr;
+        void* ye = b + U.ye;
+        int32_t* ids = reinterpret_cast<int32_t*>(ws + S.ids[u]);
+        float* wts = reinterpret_cast<float*>(ws + S.w[u]);
+        char* act = ws + S.a[u];  // the stand-in's output (rows of this ubatch from 0)
+        // layer input / output rows of this ubatch
+        const char* xin = l == 0 ? static_cast<const char*>(a->x) + t0[u] * rowb
+                                 : ws + S.pp[(l - 1) % 2] + t0[u] * rowb;
+        char* xout = l == L - 1 ? static_cast<char*>(a->out) + t0[u] * rowb : ws + S.pp[l % 2] + t0[u] * rowb;
+        const int Tu = tn[u];
+        const bool overlapped = two;
+        const int comm_grid = overlapped ? comm_cap : sms * 8;
+        const int ffn_grid = overlapped ? ffn_cap : sms * 8;
+        cudaError_t ce = cudaSuccess;
+        switch (op.op) {
+            case MOE_OP_RECORD: ce = cudaEventRecord(h->ev[op.ev], q); break;
+            case MOE_OP_WAIT: ce = cudaStreamWaitEvent(q, h->ev[op.ev], 0); break;
+            case MOE_OP_STANDIN: ce = launch_standin(c, Tu, xin, a->wa[l], act, ffn_grid, q); break;
+            case MOE_OP_ROUTE:
+                ce = launch_route(c, Tu, a->logits[l] + (size_t)t0[u] * c.num_experts, a->bias, ids, wts, comm_grid, q);
+                break;
+            case MOE_OP_PLAN:
+                ce = launch_plan(c, Tu, ids, capacity, align, counts, offsets, slot_of, token_of, err,
+                                 reinterpret_cast<int32_t*>(b + U.hist), comm_grid, q);
+                break;
+            case MOE_OP_DISPATCH: ce = launch_dispatch(c, Tu, act, slot_of, xe, xe_scale, comm_grid, q); break;
+            case MOE_OP_FFN: {
+                FfnArgs fa{counts, offsets, U.rows, xe, xe_scale, a->w13[l], fp8 ? a->w13_scale[l] : nullptr, a->w2[l],
+                           fp8 ? a->w2_scale[l] : nullptr, ye, b + U.ffn, err, two && u == 1 ? 1 : 0};
+                ce = launch_ffn(c, fa, ffn_grid, q);
+                break;
+            }
+            case MOE_OP_COMBINE: ce = launch_combine(c, Tu, ye, wts, slot_of, xout, comm_grid, q, act); break;
+        }
+        if (ce != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
 }
 
 }  // extern "C"

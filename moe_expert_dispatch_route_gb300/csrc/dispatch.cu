@@ -14,6 +14,7 @@ constexpr int kDispatchThreads = 256;
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_copy_kernel(
     int T, int kk, int nvec, const uint4* __restrict__ x, const int32_t* __restrict__ slot_of,
     uint4* __restrict__ xe) {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
@@ -44,6 +45,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_copy_kernel(
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_fp8_kernel(
     int T, int kk, int H, const uint4* __restrict__ x, const int32_t* __restrict__ slot_of,
     uint2* __restrict__ xe, float* __restrict__ xe_scale) {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int nvec = H / 8;     // 8 bf16 per 16-byte vector
@@ -95,15 +97,12 @@ cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int
     const int kk = c.top_k + c.num_shared;
     int grid = (T + 7) / 8;
     if (grid > grid_cap) grid = grid_cap;
-    if (c.dtype == MOE_FP8_E4M3) {
-        dispatch_fp8_kernel<<<grid, kDispatchThreads, 0, st>>>(
-            T, kk, c.hidden, static_cast<const uint4*>(x), slot_of, static_cast<uint2*>(xe), xe_scale);
-    } else {
-        const int nvec = c.hidden * elt_bytes(c.dtype) / 16;
-        dispatch_copy_kernel<<<grid, kDispatchThreads, 0, st>>>(
-            T, kk, nvec, static_cast<const uint4*>(x), slot_of, static_cast<uint4*>(xe));
-    }
-    return cudaGetLastError();
+    if (c.dtype == MOE_FP8_E4M3)
+        return launch_pdl(dispatch_fp8_kernel, grid, kDispatchThreads, 0, st, T, kk, c.hidden,
+                          static_cast<const uint4*>(x), slot_of, static_cast<uint2*>(xe), xe_scale);
+    const int nvec = c.hidden * elt_bytes(c.dtype) / 16;
+    return launch_pdl(dispatch_copy_kernel, grid, kDispatchThreads, 0, st, T, kk, nvec, static_cast<const uint4*>(x),
+                      slot_of, static_cast<uint4*>(xe));
 }
 
 }  // namespace moe

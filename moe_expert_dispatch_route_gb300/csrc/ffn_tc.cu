@@ -46,9 +46,17 @@ constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kNumBars * 
 constexpr int kF8Threads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 promotion + epilogue
 constexpr int kF8BK = 128;       // e4m3 elements per k-block = one 128-wide scale block
 
+// A tiles are loaded with the smallest box of 16 / 32 / 64 / 128 rows that covers the
+// tile's rows: at decode an expert has a handful of rows, and fetching 128 would
+// re-read other experts' rows (and, once the weight stream has evicted them from L2,
+// from DRAM).  The MMA still reads 128 rows of the stage; the rows past the box hold
+// stale data whose results land in accumulator rows that are never stored.
+constexpr int kNumABoxes = 4;
+__host__ __device__ constexpr int a_box_rows(int i) { return 16 << i; }
+
 struct TcParams {
-    CUtensorMap tmA;  // activations [max_rows][K] bf16
-    CUtensorMap tmB;  // weights [NE * NB][K] bf16
+    CUtensorMap tmA[kNumABoxes];  // activations [max_rows][K], box heights 16, 32, 64, 128
+    CUtensorMap tmB;              // weights [NE * NB][K]
     const int32_t* counts;
     const int32_t* offsets;
     int NE, K, kblocks;
@@ -62,6 +70,8 @@ struct TcParams {
     const float* a_scale;  // fp8: [max_rows][K/128] row-group scales of A
     const float* b_scale;  // fp8: [NE][NB/128][K/128] block scales of B
     float* out_scale;      // fp8 up: [max_rows][I/128] scales of the quantised h
+    int dense_rows;        // counts == nullptr: one dense matrix of this many rows
+    const void* resid;     // bf16 down: added to the product before rounding ([rows][H])
 };
 
 struct Smem {
@@ -140,8 +150,8 @@ __device__ void scan_tiles(const TcParams& p, const Smem& s) {
         const int e = lane * per + i;
         int v = 0;
         if (e < p.NE) {
-            int cnt = __ldg(p.counts + e);
-            const int off = __ldg(p.offsets + e);
+            int cnt = p.counts ? __ldg(p.counts + e) : p.dense_rows;
+            const int off = p.counts ? __ldg(p.offsets + e) : 0;
             if (cnt < 0 || off < 0 || (int64_t)off + cnt > p.max_rows) {
                 set_err(p.err, MOE_ERR_BAD_INDEX);
                 cnt = 0;
@@ -185,6 +195,9 @@ __device__ void producer(const TcParams& p, const Smem& s, int total) {
             b0 = t.e * p.NB + t.nt * kBN;
             b1 = b0 + 128;
         }
+        int abox = 0;
+        while (abox < kNumABoxes - 1 && a_box_rows(abox) < t.rows) ++abox;
+        const int abox_rows = a_box_rows(abox);
         for (int kb = 0; kb < p.kblocks; ++kb) {
             if (!tc::mbar_wait(&s.empty[stage], phase ^ 1u, s.abort)) {
                 ok = false;
@@ -192,8 +205,8 @@ __device__ void producer(const TcParams& p, const Smem& s, int total) {
             }
             uint8_t* a = s.stages + (size_t)stage * kStageBytes;
             uint8_t* b = a + kABytes;
-            tc::mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
-            tc::tma_load_2d(a, &p.tmA, &s.full[stage], kb * kKElems, t.row0);
+            tc::mbar_arrive_expect_tx(&s.full[stage], (uint32_t)(abox_rows * 128 + kBBytes));
+            tc::tma_load_2d(a, &p.tmA[abox], &s.full[stage], kb * kKElems, t.row0);
             tc::tma_load_2d(b, &p.tmB, &s.full[stage], kb * kKElems, b0);
             tc::tma_load_2d(b + kBBytes / 2, &p.tmB, &s.full[stage], kb * kKElems, b1);
             pending |= 1u << stage;
@@ -304,12 +317,28 @@ __device__ void epilogue(const TcParams& p, const Smem& s, int total, uint32_t t
             }
         } else {
             uint16_t* yrow = static_cast<uint16_t*>(p.out) + row * p.H + t.nt * kBN;
+            const uint16_t* rrow = p.resid ? static_cast<const uint16_t*>(p.resid) + row * p.H + t.nt * kBN : nullptr;
 #pragma unroll 1
             for (int c = 0; c < kBN; c += 32) {
                 uint32_t a[32];
                 tc::tmem_ld32(tb + c, a);
                 tc::tmem_wait_ld();
                 if (valid) {
+                    if (rrow) {  // residual: out = resid + product, one rounding
+                        const uint4* rr = reinterpret_cast<const uint4*>(rrow + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 q = rr[i];
+                            const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                a[8 * i + 2 * j] = __float_as_uint(__uint_as_float(a[8 * i + 2 * j]) +
+                                                                   bf16_bits_to_f((uint16_t)(wd[j] & 0xffffu)));
+                                a[8 * i + 2 * j + 1] = __float_as_uint(__uint_as_float(a[8 * i + 2 * j + 1]) +
+                                                                       bf16_bits_to_f((uint16_t)(wd[j] >> 16)));
+                            }
+                        }
+                    }
                     uint4 v[4];
                     uint32_t* w = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
@@ -345,13 +374,18 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_c
         tc::mbar_init(s.drain, 1);
         *s.abort = 0;
         tc::fence_barrier_init();
-        tc::prefetch_tmap(&p.tmA);
+        for (int i = 0; i < kNumABoxes; ++i) tc::prefetch_tmap(&p.tmA[i]);
         tc::prefetch_tmap(&p.tmB);
     }
     if (warp == 1) {
         tc::tmem_alloc(s.tmem_base, kTmemCols);
         tc::tmem_relinquish();
     }
+    // Everything above overlaps the previous kernel's tail.  Nothing produced upstream
+    // (counts, offsets, xe, h) is read before this wait: with a chain of such
+    // launches an earlier kernel than the immediate predecessor may still be running.
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();
     if (warp == 2) scan_tiles(p, s);
     tc::tc_fence_before();
     __syncthreads();
@@ -425,13 +459,21 @@ __device__ void mma_issuer_f8(const TcParams& p, const Smem& s, int total, uint3
     }
 }
 
-// acc[i] += partial[c0 + i] * sc for 32 columns of this thread's TMEM lane
-__device__ __forceinline__ void promote32(uint32_t taddr, float sc, float* acc) {
-    uint32_t v[32];
-    tc::tmem_ld32(taddr, v);
-    tc::tmem_wait_ld();
+// acc += partial * sc for 32 columns of this thread's TMEM lane, as packed two-wide
+// fp32 FMAs (acc[i] holds columns 2i, 2i+1).  Loaded 16 columns at a time: with 10
+// warps per SM a thread has at most 168 registers, 128 of which are accumulators.
+__device__ __forceinline__ void promote32(uint32_t taddr, float sc, float2* acc) {
+    const float2 s2 = make_float2(sc, sc);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = fmaf(__uint_as_float(v[i]), sc, acc[i]);
+    for (int h = 0; h < 2; ++h) {
+        uint32_t v[16];
+        tc::tmem_ld16(taddr + 16 * h, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[8 * h + i] =
+                __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), s2, acc[8 * h + i]);
+    }
 }
 
 template <bool kUp>
@@ -453,27 +495,41 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
         const float* bsc = p.b_scale + (size_t)t.e * (p.NB / kF8BK) * ksb;
         const int nb0 = kUp ? t.nt : 2 * t.nt + half;  // gate (up kernel) or output block
         const int nb1 = kUp ? p.I / kF8BK + t.nt : nb0;  // up block (up kernel)
-        float acc[128];
+        float2 acc[64];  // up: gate columns in acc[0..31], up columns in acc[32..63]
 #pragma unroll
-        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        // a warp whose 32 rows are all past the tile's rows has nothing to promote (at
+        // decode most tiles hold fewer than 32 rows)
+        const bool busy = q * 32 < t.rows;
+        const float* bs0 = bsc + (size_t)nb0 * ksb;
+        const float* bs1 = bsc + (size_t)nb1 * ksb;
+        // scales of the next k-block are loaded while the current one is promoted
+        float sa_n = (busy && in_rows) ? __ldg(asc) : 0.0f;
+        float sb0_n = busy ? __ldg(bs0) : 0.0f;
+        float sb1_n = (busy && kUp) ? __ldg(bs1) : 0.0f;
         for (int kb = 0; kb < p.kblocks; ++kb) {
+            const float s0 = sa_n * sb0_n, s1 = sa_n * sb1_n;
+            if (busy && kb + 1 < p.kblocks) {
+                sa_n = in_rows ? __ldg(asc + kb + 1) : 0.0f;
+                sb0_n = __ldg(bs0 + kb + 1);
+                if (kUp) sb1_n = __ldg(bs1 + kb + 1);
+            }
             if (!tc::mbar_wait(&s.tfull[pb], pph, s.abort)) {
                 ok = false;
                 break;
             }
             tc::tc_fence_after();
-            const float sa = in_rows ? __ldg(asc + kb) : 0.0f;
-            const float s0 = sa * __ldg(bsc + (size_t)nb0 * ksb + kb);
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(pb * kBN);
-            if (kUp) {
-                const float s1 = sa * __ldg(bsc + (size_t)nb1 * ksb + kb);
-                promote32(tb + 64 * half, s0, acc);
-                promote32(tb + 64 * half + 32, s0, acc + 32);
-                promote32(tb + 128 + 64 * half, s1, acc + 64);
-                promote32(tb + 128 + 64 * half + 32, s1, acc + 96);
-            } else {
+            if (busy) {
+                if (kUp) {
+                    promote32(tb + 64 * half, s0, acc);
+                    promote32(tb + 64 * half + 32, s0, acc + 16);
+                    promote32(tb + 128 + 64 * half, s1, acc + 32);
+                    promote32(tb + 128 + 64 * half + 32, s1, acc + 48);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) promote32(tb + 128 * half + 32 * c, s0, acc + 32 * c);
+                    for (int c = 0; c < 4; ++c) promote32(tb + 128 * half + 32 * c, s0, acc + 16 * c);
+                }
             }
             tc::tc_fence_before();
             __syncwarp();
@@ -484,13 +540,14 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
         if (!ok) break;
         const bool valid = r < t.rows;
         if (kUp) {
-            // h for this thread's 64 columns (gate in acc[0..63], up in acc[64..127])
+            // h for this thread's 64 columns (written over the gate pairs)
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const float g = acc[i];
-                acc[i] = g / (1.0f + expf(-g)) * acc[64 + i];
-                amax = fmaxf(amax, fabsf(acc[i]));
+            for (int i = 0; i < 32; ++i) {
+                const float g0 = acc[i].x, g1 = acc[i].y;
+                acc[i].x = g0 / (1.0f + expf(-g0)) * acc[32 + i].x;
+                acc[i].y = g1 / (1.0f + expf(-g1)) * acc[32 + i].y;
+                amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
             }
             // the row's other 64 columns belong to the partner thread: exchange amax
             ++seq;
@@ -513,8 +570,8 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const uint16_t lo = f2_to_e4m3x2(scalbnf(acc[4 * i], -se), scalbnf(acc[4 * i + 1], -se));
-                    const uint16_t hi = f2_to_e4m3x2(scalbnf(acc[4 * i + 2], -se), scalbnf(acc[4 * i + 3], -se));
+                    const uint16_t lo = f2_to_e4m3x2(scalbnf(acc[2 * i].x, -se), scalbnf(acc[2 * i].y, -se));
+                    const uint16_t hi = f2_to_e4m3x2(scalbnf(acc[2 * i + 1].x, -se), scalbnf(acc[2 * i + 1].y, -se));
                     w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + row * p.I + t.nt * 128 + 64 * half);
@@ -526,9 +583,9 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
             uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.H + t.nt * kBN + 128 * half);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                dst[i] = make_uint4(pack_bf16x2(acc[8 * i], acc[8 * i + 1]), pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
-                                    pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]),
-                                    pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
+                dst[i] = make_uint4(pack_bf16x2(acc[4 * i].x, acc[4 * i].y), pack_bf16x2(acc[4 * i + 1].x, acc[4 * i + 1].y),
+                                    pack_bf16x2(acc[4 * i + 2].x, acc[4 * i + 2].y),
+                                    pack_bf16x2(acc[4 * i + 3].x, acc[4 * i + 3].y));
         }
     }
     if (!ok) fail(s, p.err);
@@ -551,7 +608,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_
         tc::mbar_init(s.drain, 1);
         *s.abort = 0;
         tc::fence_barrier_init();
-        tc::prefetch_tmap(&p.tmA);
+        for (int i = 0; i < kNumABoxes; ++i) tc::prefetch_tmap(&p.tmA[i]);
         tc::prefetch_tmap(&p.tmB);
     }
     for (int i = threadIdx.x; i < 256; i += blockDim.x) s.xseq[i] = 0;
@@ -559,6 +616,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_
         tc::tmem_alloc(s.tmem_base, kTmemCols);
         tc::tmem_relinquish();
     }
+    tc::pdl_launch_dependents();
+    tc::pdl_wait();  // see the bf16 kernel: nothing from upstream is read before this
     if (warp == 2) scan_tiles(p, s);
     tc::tc_fence_before();
     __syncthreads();
@@ -596,14 +655,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D K-major matrix [rows][inner] with the 128-byte swizzle and a box of one
-// 128-byte row (64 bf16 or 128 e4m3) by 128 rows.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, bool fp8) {
+// 128-byte row (64 bf16 or 128 e4m3) by box_rows rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, bool fp8, int box_rows = 128) {
     auto enc = encode_fn();
     if (!enc) return false;
     const uint64_t elt = fp8 ? 1 : 2;
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {inner * elt};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), 128};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
                dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -620,8 +679,20 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    kern<<<grid, kFp8 ? kF8Threads : kThreads, kSmemBytes, st>>>(p);
-    return cudaGetLastError();
+    // programmatic dependent launch: this kernel's prologue may overlap the tail of the
+    // previous kernel on the stream; it waits (griddepcontrol.wait) before reading
+    // anything that kernel wrote
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kFp8 ? kF8Threads : kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
@@ -644,9 +715,10 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
         fp8 ? reinterpret_cast<float*>(static_cast<char*>(a.ws) + align_up((size_t)a.max_rows * I, 256)) : nullptr;
     const int kelems = fp8 ? kF8BK : kBK;
     TcParams up{};
-    if (!make_map(&up.tmA, a.xe, (uint64_t)H, (uint64_t)a.max_rows, fp8) ||
-        !make_map(&up.tmB, a.w13, (uint64_t)H, (uint64_t)NE * 2 * I, fp8))
-        return cudaErrorInvalidValue;
+    for (int i = 0; i < kNumABoxes; ++i)
+        if (!make_map(&up.tmA[i], a.xe, (uint64_t)H, (uint64_t)a.max_rows, fp8, a_box_rows(i)))
+            return cudaErrorInvalidValue;
+    if (!make_map(&up.tmB, a.w13, (uint64_t)H, (uint64_t)NE * 2 * I, fp8)) return cudaErrorInvalidValue;
     up.counts = a.counts;
     up.offsets = a.offsets;
     up.NE = NE;
@@ -664,9 +736,10 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     up.b_scale = a.w13_scale;
     up.out_scale = h_scale;
     TcParams dn = up;
-    if (!make_map(&dn.tmA, h, (uint64_t)I, (uint64_t)a.max_rows, fp8) ||
-        !make_map(&dn.tmB, a.w2, (uint64_t)I, (uint64_t)NE * H, fp8))
-        return cudaErrorInvalidValue;
+    for (int i = 0; i < kNumABoxes; ++i)
+        if (!make_map(&dn.tmA[i], h, (uint64_t)I, (uint64_t)a.max_rows, fp8, a_box_rows(i)))
+            return cudaErrorInvalidValue;
+    if (!make_map(&dn.tmB, a.w2, (uint64_t)I, (uint64_t)NE * H, fp8)) return cudaErrorInvalidValue;
     dn.K = I;
     dn.kblocks = I / kelems;
     dn.NB = H;
@@ -678,6 +751,41 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     cudaError_t e = fp8 ? launch_one<true, true>(up, grid, st) : launch_one<true, false>(up, grid, st);
     if (e != cudaSuccess) return e;
     return fp8 ? launch_one<false, true>(dn, grid, st) : launch_one<false, false>(dn, grid, st);
+}
+
+bool standin_tc_supported(const moe_config& c) {
+    const DeviceInfo& d = device_info();
+    return c.dtype != MOE_F32 && d.cc_major == 10 && c.hidden % kBN == 0 && d.smem_optin >= kSmemBytes &&
+           encode_fn() != nullptr;
+}
+
+// out[rows][H] = x + x . Wa^T (bf16, fp32 accumulation): the down kernel on one dense
+// "expert" with a residual epilogue.
+cudaError_t launch_standin(const moe_config& c, int rows, const void* x, const void* wa, void* out, int grid_cap,
+                           cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    const int H = c.hidden;
+    int grid = device_info().num_sms;
+    if (grid > grid_cap) grid = grid_cap;
+    if (grid < 1) grid = 1;
+    TcParams p{};
+    for (int i = 0; i < kNumABoxes; ++i)
+        if (!make_map(&p.tmA[i], x, (uint64_t)H, (uint64_t)rows, false, a_box_rows(i))) return cudaErrorInvalidValue;
+    if (!make_map(&p.tmB, wa, (uint64_t)H, (uint64_t)H, false)) return cudaErrorInvalidValue;
+    p.counts = nullptr;
+    p.offsets = nullptr;
+    p.dense_rows = rows;
+    p.NE = 1;
+    p.K = H;
+    p.kblocks = H / kBK;
+    p.NB = H;
+    p.ntn = H / kBN;
+    p.I = H;
+    p.H = H;
+    p.max_rows = rows;
+    p.out = out;
+    p.resid = x;
+    return launch_one<false, false>(p, grid, st);
 }
 
 }  // namespace moe

@@ -34,7 +34,8 @@ cudaError_t launch_plan(const moe_config& c, int T, const int32_t* ids, int capa
 cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int32_t* slot_of,
                             void* xe, float* xe_scale, int grid_cap, cudaStream_t st);
 cudaError_t launch_combine(const moe_config& c, int T, const void* ye, const float* w,
-                           const int32_t* slot_of, void* y, int grid_cap, cudaStream_t st);
+                           const int32_t* slot_of, void* y, int grid_cap, cudaStream_t st,
+                           const void* resid = nullptr);
 
 // FFN: scratch = h [max_rows][I] (+ fp8 scales) followed by the kernels' own scratch.
 size_t ffn_scratch_bytes(const moe_config& c, int64_t max_rows);
@@ -61,6 +62,28 @@ cudaError_t launch_ffn_simt(const moe_config& c, const FfnArgs& a, int grid_cap,
 // ffn_tc.cu: tcgen05 / TMEM / TMA grouped GEMM (bf16 layers)
 bool ffn_tc_supported(const moe_config& c);
 cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
+// the stand-in for a layer's non-MoE compute in a stack: out = x + x . Wa^T (bf16)
+bool standin_tc_supported(const moe_config& c);
+cudaError_t launch_standin(const moe_config& c, int rows, const void* x, const void* wa, void* out, int grid_cap,
+                           cudaStream_t st);
+
+// Launches `kern` with programmatic stream serialisation: it may be scheduled while
+// the previous kernel on the stream finishes; the kernel calls pdl_begin() before it
+// touches that kernel's outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ((KArgs)args)...);
+}
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int elt_bytes(int dtype) { return dtype == MOE_F32 ? 4 : dtype == MOE_BF16 ? 2 : 1; }

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(int T, int k, 
                                                                   const int32_t* __restrict__ ids,
                                                                   int32_t* __restrict__ hist) {
     __shared__ int h[kMaxExperts];
+    pdl_begin();
     const int NE = E + S, kk = k + S;
     for (int e = threadIdx.x; e < NE; e += blockDim.x) h[e] = 0;
     __syncthreads();
@@ -109,6 +110,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_assign_kernel(
     __shared__ int off[kMaxExperts + 1];
     __shared__ int wcnt[kPlanWarps][kMaxExperts];
     __shared__ int warp_tot[kPlanWarps + 1];
+    extern __shared__ int chunk_e[];  // this chunk's entry experts (-1 = bad id)
+    pdl_begin();
 
     const int NE = E + S, kk = k + S;
     const int chunk = blockIdx.x;
@@ -126,9 +129,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_assign_kernel(
         __syncthreads();
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
             int e = entry_expert(ids, t0 + i / kk, i % kk, k, E);
+            chunk_e[i] = e;
             if (e >= 0) atomicAdd(&total[e], 1);
         }
     } else {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) chunk_e[i] = entry_expert(ids, t0 + i / kk, i % kk, k, E);
         for (int e = threadIdx.x; e < NE; e += blockDim.x) {
             int tot = 0, bef = 0;
             for (int c = 0; c < nchunks; ++c) {
@@ -156,10 +161,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_assign_kernel(
             counts[e] = capacity > 0 ? min(total[e], capacity) : total[e];
         for (int e = threadIdx.x; e <= NE; e += blockDim.x) offsets[e] = off[e];
     }
-    // padding rows of the experts this CTA owns (e = chunk mod nchunks) are marked -1
-    for (int e = chunk; e < NE; e += nchunks) {
-        int used = capacity > 0 ? min(total[e], capacity) : total[e];
-        for (int r = off[e] + used + threadIdx.x; r < off[e + 1]; r += blockDim.x) token_of[r] = -1;
+    // padding rows are marked -1; CTA c takes every nchunks-th block of 256 rows and
+    // finds each row's expert by binary search over the offsets
+    for (int r = (chunk * kPlanThreads) + threadIdx.x; r < off[NE]; r += nchunks * kPlanThreads) {
+        int lo = 0, hi = NE - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off[mid] <= r) lo = mid;
+            else hi = mid - 1;
+        }
+        const int used = capacity > 0 ? min(total[lo], capacity) : total[lo];
+        if (r >= off[lo] + used) token_of[r] = -1;
     }
     for (int e = threadIdx.x; e < NE; e += blockDim.x) base[e] += off[e];
     __syncthreads();
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_assign_kernel(
         const int i = it + threadIdx.x;
         const bool in = i < n;
         const int t = t0 + (in ? i / kk : 0), j = in ? i % kk : 0;
-        int e = in ? entry_expert(ids, t, j, k, E) : -1;
+        int e = in ? chunk_e[i] : -1;
         const bool good = in && e >= 0;
         if (in && !good) {
             slot_of[(size_t)t * kk + j] = -1;
@@ -209,13 +221,15 @@ cudaError_t launch_plan(const moe_config& c, int T, const int32_t* ids, int capa
     const int tpc = plan_tokens_per_chunk(c);
     int nchunks = (T + tpc - 1) / tpc;
     if (nchunks < 1) nchunks = 1;  // T == 0 still writes counts and offsets
-    if (nchunks > 1)
-        plan_count_kernel<<<nchunks, kPlanThreads, 0, st>>>(T, c.top_k, c.num_shared, c.num_experts, tpc,
-                                                            ids, hist_ws);
-    plan_assign_kernel<<<nchunks, kPlanThreads, 0, st>>>(T, c.top_k, c.num_shared, c.num_experts, tpc,
-                                                         nchunks, capacity, align, ids, hist_ws, counts,
-                                                         offsets, slot_of, token_of, err);
-    return cudaGetLastError();
+    if (nchunks > 1) {
+        cudaError_t e = launch_pdl(plan_count_kernel, nchunks, kPlanThreads, 0, st, T, c.top_k, c.num_shared,
+                                   c.num_experts, tpc, ids, hist_ws);
+        if (e != cudaSuccess) return e;
+    }
+    const size_t ids_smem = (size_t)tpc * (c.top_k + c.num_shared) * sizeof(int);
+    return launch_pdl(plan_assign_kernel, nchunks, kPlanThreads, ids_smem, st, T, c.top_k, c.num_shared,
+                      c.num_experts, tpc, nchunks, capacity, align, ids, (const int32_t*)hist_ws, counts, offsets,
+                      slot_of, token_of, err);
 }
 
 }  // namespace moe

@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(256) route_softmax_kernel(int T, int E, int k,
                                                             const float* __restrict__ logits,
                                                             int32_t* __restrict__ ids,
                                                             float* __restrict__ w) {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(256) route_grouped_kernel(int T, int E, int k,
                                                             int32_t* __restrict__ ids,
                                                             float* __restrict__ w) {
     extern __shared__ float route_smem[];
+    pdl_begin();
     float* cs = route_smem + (threadIdx.x >> 5) * E;  // this warp's choice scores
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -204,16 +206,12 @@ __global__ void __launch_bounds__(256) route_grouped_kernel(int T, int E, int k,
 template <int NPER>
 static cudaError_t launch_route_n(const moe_config& c, int T, const float* logits, const float* bias,
                                   int32_t* ids, float* w, int grid, cudaStream_t st) {
-    if (c.gate == MOE_GATE_SOFTMAX) {
-        route_softmax_kernel<NPER><<<grid, 256, 0, st>>>(T, c.num_experts, c.top_k, c.renormalize,
-                                                        logits, ids, w);
-    } else {
-        size_t smem = sizeof(float) * 8 * c.num_experts;
-        route_grouped_kernel<NPER><<<grid, 256, smem, st>>>(T, c.num_experts, c.top_k, c.n_group,
-                                                            c.topk_group, c.renormalize,
-                                                            c.routed_scale, logits, bias, ids, w);
-    }
-    return cudaGetLastError();
+    if (c.gate == MOE_GATE_SOFTMAX)
+        return launch_pdl(route_softmax_kernel<NPER>, grid, 256, 0, st, T, c.num_experts, c.top_k, c.renormalize,
+                          logits, ids, w);
+    const size_t smem = sizeof(float) * 8 * c.num_experts;
+    return launch_pdl(route_grouped_kernel<NPER>, grid, 256, smem, st, T, c.num_experts, c.top_k, c.n_group,
+                      c.topk_group, c.renormalize, c.routed_scale, logits, bias, ids, w);
 }
 
 cudaError_t launch_route(const moe_config& c, int T, const float* logits, const float* bias,

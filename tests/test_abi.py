@@ -128,3 +128,60 @@ def test_unsplit_schedule_is_one_stream():
     s = B.moe_dbo_schedule(False)
     assert [B.OPS[o[1]] for o in s] == ["route", "plan", "dispatch", "ffn", "combine"]
     assert all(o[0] == 0 for o in s)
+
+
+def _graph(sched):
+    """Dependency edges of an enqueue schedule: stream order plus event waits (a wait
+    depends on the op recorded just before the latest record of that event)."""
+    ops = [(st, B.OPS[op], ub, ev) for st, op, ub, ev in sched]
+    deps = {i: set() for i in range(len(ops))}
+    last_on = {}
+    last_rec = {}
+    for i, (st, name, ub, ev) in enumerate(ops):
+        if st in last_on:
+            deps[i].add(last_on[st])
+        if name == "wait":
+            deps[i].add(last_rec[ev])
+        if name == "record":
+            last_rec[ev] = i
+        last_on[st] = i
+    return ops, deps
+
+
+def _ancestors(deps, i):
+    seen, todo = set(), [i]
+    while todo:
+        j = todo.pop()
+        for d in deps[j]:
+            if d not in seen:
+                seen.add(d)
+                todo.append(d)
+    return seen
+
+
+def _find(ops, name, ub, nth=0):
+    return [i for i, o in enumerate(ops) if o[1] == name and o[2] == ub][nth]
+
+
+def test_stack_schedule_overlap_rule_and_prefix_variant():
+    L = 3
+    for before in (True, False):
+        ops, deps = _graph(B.moe_stack_schedule(L, True, before))
+        for l in range(L):
+            a0, a1 = _find(ops, "standin", 0, l), _find(ops, "standin", 1, l)
+            d0 = _find(ops, "dispatch", 0, l)
+            f0, f1 = _find(ops, "ffn", 0, l), _find(ops, "ffn", 1, l)
+            c0, c1 = _find(ops, "combine", 0, l), _find(ops, "combine", 1, l)
+            anc_d0, anc_c0 = _ancestors(deps, d0), _ancestors(deps, c0)
+            # data dependencies hold in both placements
+            assert a0 in anc_d0 and d0 in _ancestors(deps, f0) and f0 in anc_c0
+            assert f1 in _ancestors(deps, c1)
+            if l + 1 < L:
+                assert c0 in _ancestors(deps, _find(ops, "standin", 0, l + 1))
+            # the fix: dispatch(0) does not wait for the other ubatch's stand-in, and
+            # combine(0) not for the other ubatch's experts; the old placement does
+            assert (a1 not in anc_d0) == before
+            assert (f1 not in anc_c0) == before
+        # everything joins back to the compute stream
+        assert ops[-1][0] == 0 and ops[-1][1] == "wait"
+    assert all(o[0] == 0 for o in B.moe_stack_schedule(2, False, True))
