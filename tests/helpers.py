@@ -42,14 +42,20 @@ def np_weights(W: dict, experts=None) -> dict:
     return out
 
 
-def check_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
+# The stack's output is a residual stream of magnitude O(1..10), where one bf16 step
+# exceeds the layer's absolute bound: relative L2 1e-2 and max-abs 2^-6 of the largest
+# value (two bf16 steps there).
+TOL_STACK = dict(max_abs=None, max_abs_rel=2.0 ** -6, rel_l2=1e-2)
+
+
+def check_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "", tol=None):
     got = got.astype(np.float64)
     ref = ref.astype(np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     diff = got - ref
     rel = float(np.linalg.norm(diff) / max(np.linalg.norm(ref), 1e-30))
-    tol = TOL[dtype]
+    tol = tol or TOL[dtype]
     assert rel <= tol["rel_l2"], f"{what}: relative L2 {rel:.3e} > {tol['rel_l2']}"
     if tol.get("max_abs") is not None:
         mx = float(np.max(np.abs(diff))) if diff.size else 0.0

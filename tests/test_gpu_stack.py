@@ -10,7 +10,7 @@ from moe_expert_dispatch_route_gb300 import binding as B
 from moe_expert_dispatch_route_gb300 import synth
 from moe_expert_dispatch_route_gb300 import workloads as W
 
-from helpers import check_close, np_f32, np_weights, ocfg
+from helpers import TOL_STACK, check_close, np_f32, np_weights, ocfg
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -69,7 +69,8 @@ def test_stack_matches_oracle(wl, L):
     got = S.run()
     ref = S.oracle(wl.split)
     assert ref["status"] == 0
-    check_close(got, ref["y"], wl.dtype, f"stack of {L}")
+    tol = dict(TOL_STACK, rel_l2=3e-2) if wl.dtype == "fp8" else TOL_STACK
+    check_close(got, ref["y"], wl.dtype, f"stack of {L}", tol)
     S.close()
 
 
