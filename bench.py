@@ -466,12 +466,48 @@ def ffn_roofline(B, wl, cfg, inp, dev, args, comm_sms, compute):
     else:
         achieved, peak, unit = flops_alg / t / 1e12, tf / 1e12, "TFLOP/s"
     traffic = profiled_traffic("ffn", wl.name)
+
+    # the comm-side kernels of the same ubatch, each timed alone on the whole GPU
+    def time_call(fn, n_iter):
+        with torch.cuda.stream(compute):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(compute):
+            a0.record(compute)
+            for _ in range(n_iter):
+                fn()
+            a1.record(compute)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / n_iter / 1e3
+
+    y0 = torch.zeros(T0, H * io, dtype=torch.uint8, device=dev)
+    n_iter = max(20, args.steps)
+    kern = {}
+    specs = {
+        "route": (lambda: B.moe_route(cfg, T0, inp["logits"], None, ids, w, 0, compute),
+                  T0 * E * 4 + T0 * k * 8),
+        "plan": (lambda: B.moe_plan(cfg, T0, ids, wl.capacity, wl.align, counts, offsets, slot_of, token_of, err,
+                                    pws, pws.numel(), 0, compute),
+                 T0 * k * 4 + T0 * kk * 4 + rows * 4 + (2 * NE + 1) * 4),
+        "dispatch": (lambda: B.moe_dispatch(cfg, T0, inp["x"], slot_of, xe, xs, 0, compute),
+                     T0 * H * io + T0 * kk * 4 + used * H * elt + (used * (H // 128) * 4 if fp8 else 0)),
+        "combine": (lambda: B.moe_combine(cfg, T0, ye, w, slot_of, y0, 0, compute),
+                    used * H * io + T0 * H * io + T0 * kk * 4 + T0 * k * 4),
+    }
+    for name, (fn, nbytes) in specs.items():
+        tk = time_call(fn, n_iter)
+        kern[name] = {"us": round(tk * 1e6, 3), "algorithmic_bytes": int(nbytes),
+                      "achieved_gbs": round(nbytes / tk / 1e9, 1), "frac_hbm": round(nbytes / tk / bw, 4)}
+    torch.cuda.synchronize()
     return {"kernel": "moe_expert_ffn (gate/up + SwiGLU, down) on ubatch 0", "bound": bound,
             "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": unit,
             "frac": round(achieved / peak, 4), "peak_source": f"{src} ({'fp8 = 2x bf16 nominal ratio' if fp8 and bound == 'tensor' else 'burst'})",
             "traffic": traffic, "algorithmic_bytes": int(bytes_alg), "algorithmic_flops": flops_alg,
             "us_per_launch": round(t * 1e6, 3), "rows": used, "experts_touched": touched,
-            "ctas": ffn_ctas}
+            "ctas": ffn_ctas, "comm_kernels": kern}
 
 
 def run_e2e(B, wl, cfg, inp, args_c, handle, comm, compute, enqueue, logits, x, y, args, world):

@@ -138,7 +138,8 @@ MOE_API moe_status moe_route(const moe_config* cfg, int32_t T, const float* logi
  * topk_ids device int32 [T][k].
  * counts   device int32 [E+S] (out); offsets device int32 [E+S+1] (out).
  * slot_of  device int32 [T][k+S] (out): row of each entry, -1 if not placed.
- * token_of device int32 [moe_plan_rows(...)] (out): token of each row, -1 = padding.
+ * token_of device int32 [moe_plan_rows(...)] (out, may be NULL when not wanted): token of
+ *          each row, -1 = padding.
  * err_flag device int32 (required): MOE_ERR_BAD_INDEX / MOE_ERR_CAPACITY.
  * ws       device scratch of moe_plan_workspace_size(cfg, T) bytes (may be NULL when
  *          that is 0). */

@@ -129,8 +129,7 @@ moe_status moe_plan(const moe_config* cfg, int32_t T, const int32_t* topk_ids, i
     moe_status s = check_config(cfg);
     if (s != MOE_OK) return s;
     if (T < 0 || capacity < 0 || align < 1) return MOE_ERR_INVALID_ARG;
-    if (!counts || !offsets || !err_flag || (T > 0 && (!topk_ids || !slot_of || !token_of)))
-        return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !err_flag || (T > 0 && (!topk_ids || !slot_of))) return MOE_ERR_INVALID_ARG;
     if ((int64_t)moe_plan_rows(cfg, T, capacity, align) > (int64_t)INT32_MAX) return MOE_ERR_INVALID_ARG;
     const size_t need = moe_plan_workspace_size(cfg, T);
     if (need > 0 && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;

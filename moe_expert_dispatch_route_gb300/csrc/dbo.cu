@@ -135,7 +135,7 @@ std::vector<Op> make_stack_schedule(int L, bool two, bool before_yield) {
 
 // Byte layout of one ubatch's slice of the layer workspace.
 struct UbLayout {
-    size_t counts, offsets, slot_of, token_of, hist, xe, xe_scale, ye, ffn, total;
+    size_t counts, offsets, slot_of, hist, xe, xe_scale, ye, ffn, total;
     int64_t rows;
 };
 
@@ -154,7 +154,6 @@ UbLayout ub_layout(const moe_config& c, int T, int capacity, int align) {
     L.counts = take(NE * 4);
     L.offsets = take((NE + 1) * 4);
     L.slot_of = take((size_t)T * kk * 4);
-    L.token_of = take((size_t)L.rows * 4);
     L.hist = take(moe_plan_workspace_size(&c, T));
     L.xe = take((size_t)L.rows * H * elt_bytes(c.dtype));
     L.xe_scale = take(c.dtype == MOE_FP8_E4M3 ? (size_t)L.rows * (H / 128) * 4 : 0);
@@ -264,7 +263,6 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
         int32_t* counts = reinterpret_cast<int32_t*>(b + L.counts);
         int32_t* offsets = reinterpret_cast<int32_t*>(b + L.offsets);
         int32_t* slot_of = reinterpret_cast<int32_t*>(b + L.slot_of);
-        int32_t* token_of = reinterpret_cast<int32_t*>(b + L.token_of);
         void* xe = b + L.xe;
         float* xe_scale = c.dtype == MOE_FP8_E4M3 ? reinterpret_cast<float*>(b + L.xe_scale) : nullptr;
         void* ye = b + L.ye;
@@ -283,7 +281,7 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
             case MOE_OP_WAIT: ce = cudaStreamWaitEvent(q, h->ev[op.ev], 0); break;
             case MOE_OP_ROUTE: ce = launch_route(c, Tu, logits_u, a->bias, ids_u, w_u, comm_grid, q); break;
             case MOE_OP_PLAN:
-                ce = launch_plan(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, token_of, err,
+                ce = launch_plan(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, nullptr, err,
                                  reinterpret_cast<int32_t*>(b + L.hist), comm_grid, q);
                 break;
             case MOE_OP_DISPATCH: {
@@ -409,7 +407,6 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
         int32_t* counts = reinterpret_cast<int32_t*>(b + U.counts);
         int32_t* offsets = reinterpret_cast<int32_t*>(b + U.offsets);
         int32_t* slot_of = reinterpret_cast<int32_t*>(b + U.slot_of);
-        int32_t* token_of = reinterpret_cast<int32_t*>(b + U.token_of);
         void* xe = b + U.xe;
         float* xe_scale = fp8 ? reinterpret_cast<float*>(b + U.xe_scale) : nullptr;
         void* ye = b + U.ye;
@@ -433,7 +430,7 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
                 ce = launch_route(c, Tu, a->logits[l] + (size_t)t0[u] * c.num_experts, a->bias, ids, wts, comm_grid, q);
                 break;
             case MOE_OP_PLAN:
-                ce = launch_plan(c, Tu, ids, capacity, align, counts, offsets, slot_of, token_of, err,
+                ce = launch_plan(c, Tu, ids, capacity, align, counts, offsets, slot_of, nullptr, err,
                                  reinterpret_cast<int32_t*>(b + U.hist), comm_grid, q);
                 break;
             case MOE_OP_DISPATCH: ce = launch_dispatch(c, Tu, act, slot_of, xe, xe_scale, comm_grid, q); break;

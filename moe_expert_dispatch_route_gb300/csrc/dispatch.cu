@@ -53,13 +53,16 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_fp8_kernel(
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
         const int my_slot = lane < kk ? __ldg(slot_of + (size_t)t * kk + lane) : -1;
         const uint4* src = x + (size_t)t * nvec;
+        // the row is read ahead one pass (two 16-byte loads a lane in flight)
+        uint4 next = lane < nvec ? __ldg(src + lane) : make_uint4(0u, 0u, 0u, 0u);
         for (int v = lane; v - lane < nvec; v += 32) {
             // H is a multiple of 128, so a half-warp is either fully inside or fully out
             const bool in = v < nvec;
             float f[8];
             float amax = 0.0f;
+            const uint4 raw = next;
+            if (v + 32 < nvec) next = __ldg(src + v + 32);
             if (in) {
-                uint4 raw = __ldg(src + v);
                 const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {

@@ -161,17 +161,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_assign_kernel(
             counts[e] = capacity > 0 ? min(total[e], capacity) : total[e];
         for (int e = threadIdx.x; e <= NE; e += blockDim.x) offsets[e] = off[e];
     }
-    // padding rows are marked -1; CTA c takes every nchunks-th block of 256 rows and
-    // finds each row's expert by binary search over the offsets
-    for (int r = (chunk * kPlanThreads) + threadIdx.x; r < off[NE]; r += nchunks * kPlanThreads) {
-        int lo = 0, hi = NE - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (off[mid] <= r) lo = mid;
-            else hi = mid - 1;
+    // padding rows are marked -1 (when the caller wants token_of): one warp per expert,
+    // experts dealt round-robin over the CTAs' warps
+    if (token_of) {
+        for (int e = chunk * kPlanWarps + warp; e < NE; e += nchunks * kPlanWarps) {
+            const int used = capacity > 0 ? min(total[e], capacity) : total[e];
+            for (int r = off[e] + used + lane; r < off[e + 1]; r += 32) token_of[r] = -1;
         }
-        const int used = capacity > 0 ? min(total[lo], capacity) : total[lo];
-        if (r >= off[lo] + used) token_of[r] = -1;
     }
     for (int e = threadIdx.x; e < NE; e += blockDim.x) base[e] += off[e];
     __syncthreads();
@@ -200,7 +196,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_assign_kernel(
             if (capacity > 0 && row - off[e] >= capacity) {
                 slot = -1;
                 set_err(err, MOE_ERR_CAPACITY);
-            } else {
+            } else if (token_of) {
                 token_of[row] = t;
             }
             slot_of[(size_t)t * kk + j] = slot;

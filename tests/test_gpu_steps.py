@@ -259,3 +259,23 @@ def test_combine_skips_unplaced_entries():
                   torch.as_tensor(p["slot_of"], device=DEV), y)
     torch.cuda.synchronize()
     check_close(np_f32(y), ref, "bf16", "y")
+
+
+def test_plan_without_token_of_gives_the_same_plan():
+    wl = W.DSV2LITE.with_(T=4096)
+    cfg = B.config_of(wl)
+    logits = synth.logits(wl.T, wl.num_experts, wl.routing, wl.seed)
+    ids, _ = oracle.route(ocfg(wl), logits.numpy())
+    ref = _plan_gpu(wl, ids, wl.T, 0, 128)
+    NE, kk = wl.num_experts + wl.num_shared, wl.top_k + wl.num_shared
+    counts = torch.zeros(NE, dtype=torch.int32, device=DEV)
+    offsets = torch.zeros(NE + 1, dtype=torch.int32, device=DEV)
+    slot_of = torch.zeros(wl.T, kk, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    wsb = B.moe_plan_workspace_size(cfg, wl.T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    B.moe_plan(cfg, wl.T, torch.as_tensor(ids, device=DEV), 0, 128, counts, offsets, slot_of, None, err, ws, wsb)
+    torch.cuda.synchronize()
+    assert np.array_equal(counts.cpu().numpy(), ref["counts"])
+    assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(slot_of.cpu().numpy(), ref["slot_of"])
