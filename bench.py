@@ -467,21 +467,25 @@ def ffn_roofline(B, wl, cfg, inp, dev, args, comm_sms, compute):
         achieved, peak, unit = flops_alg / t / 1e12, tf / 1e12, "TFLOP/s"
     traffic = profiled_traffic("ffn", wl.name)
 
-    # the comm-side kernels of the same ubatch, each timed alone on the whole GPU
+    # the comm-side kernels of the same ubatch, each timed alone on the whole GPU, one
+    # call at a time between CUDA events with L2 flushed before each call (their
+    # working sets can be smaller than L2)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
     def time_call(fn, n_iter):
         with torch.cuda.stream(compute):
             for _ in range(3):
                 fn()
         torch.cuda.synchronize()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_iter)]
         with torch.cuda.stream(compute):
-            a0.record(compute)
-            for _ in range(n_iter):
+            for a0, a1 in evs:
+                flush.zero_()
+                a0.record(compute)
                 fn()
-            a1.record(compute)
+                a1.record(compute)
         torch.cuda.synchronize()
-        return a0.elapsed_time(a1) / n_iter / 1e3
+        return sum(a0.elapsed_time(a1) for a0, a1 in evs) / n_iter / 1e3
 
     y0 = torch.zeros(T0, H * io, dtype=torch.uint8, device=dev)
     n_iter = max(20, args.steps)
@@ -507,7 +511,8 @@ def ffn_roofline(B, wl, cfg, inp, dev, args, comm_sms, compute):
             "frac": round(achieved / peak, 4), "peak_source": f"{src} ({'fp8 = 2x bf16 nominal ratio' if fp8 and bound == 'tensor' else 'burst'})",
             "traffic": traffic, "algorithmic_bytes": int(bytes_alg), "algorithmic_flops": flops_alg,
             "us_per_launch": round(t * 1e6, 3), "rows": used, "experts_touched": touched,
-            "ctas": ffn_ctas, "comm_kernels": kern}
+            "ctas": ffn_ctas, "comm_kernels": kern,
+            "comm_kernels_note": "each timed alone, whole GPU, L2 flushed before every call"}
 
 
 def run_e2e(B, wl, cfg, inp, args_c, handle, comm, compute, enqueue, logits, x, y, args, world):

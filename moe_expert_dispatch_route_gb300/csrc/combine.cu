@@ -1,7 +1,7 @@
-// moe_combine kernel: one warp per token gathers its k+S expert-output rows with
-// 16-byte loads, accumulates w_j * ye in fp32 in the fixed (j, then s) order
-// (optionally starting from a residual row) and stores the row once.  Each lane
-// handles two 16-byte column blocks per pass, so up to 16 row loads are in flight.
+// moe_combine kernel: a warp takes one token's slice of 64 16-byte column blocks,
+// gathers the token's k+S expert-output rows there with 16-byte loads (two blocks a
+// lane, up to 16 row loads in flight), accumulates w_j * ye in fp32 in the fixed
+// (j, then s) order (optionally starting from a residual row) and stores once.
 // No atomics: every output element is written by exactly one lane.
 #include "common.cuh"
 #include "kernels.h"
@@ -34,10 +34,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     constexpr int kV = 2;               // column blocks per lane per pass
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    // work item = (token, slice of 32 * kV column blocks): small batches still spread
+    // over many warps
+    const int nslices = (nvec + 32 * kV - 1) / (32 * kV);
+    const int items = T * nslices;
+    for (int it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += nwarps) {
+        const int t = it / nslices;
+        const int v0 = (it - t * nslices) * 32 * kV;
         const int my_slot = lane < kk ? __ldg(slot_of + (size_t)t * kk + lane) : -1;
         const float my_w = lane < k ? __ldg(w + (size_t)t * k + lane) : 1.0f;
-        for (int v0 = 0; v0 < nvec; v0 += 32 * kV) {
+        {
             float acc[kV][kPer];
 #pragma unroll
             for (int b = 0; b < kV; ++b) {
@@ -98,7 +104,8 @@ cudaError_t launch_combine(const moe_config& c, int T, const void* ye, const flo
     if (T <= 0) return cudaSuccess;
     const int kk = c.top_k + c.num_shared;
     const int nvec = c.hidden * io_bytes(c.dtype) / 16;
-    int grid = (T + 7) / 8;
+    const long items = (long)T * ((nvec + 63) / 64);
+    int grid = (int)((items + 7) / 8);
     if (grid > grid_cap) grid = grid_cap;
     if (c.dtype == MOE_F32)
         return launch_pdl(combine_kernel<true>, grid, kCombineThreads, 0, st, T, c.top_k, kk, nvec,

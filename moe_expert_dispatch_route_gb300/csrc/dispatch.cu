@@ -1,6 +1,6 @@
-// moe_dispatch kernels: one warp per token; the token row is read once with 16-byte
-// coalesced loads and written to each of its k+S destination rows with 16-byte
-// (8-byte for fp8) stores.  FP8 layers quantise each 1x128 group on the fly: a
+// moe_dispatch kernels: a warp takes one token's slice of 128 16-byte vectors; the
+// slice is read once with coalesced 16-byte loads and written to each of the token's
+// k+S destination rows with 16-byte (8-byte for fp8) stores.  FP8 layers quantise each 1x128 group on the fly: a
 // half-warp owns one group (16 lanes x 8 bf16), reduces its amax with four
 // shuffles and converts with cvt.rn.satfinite.e4m3x2.
 #include "common.cuh"
@@ -17,10 +17,15 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_copy_kernel(
     pdl_begin();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    // work item = (token, slice of 128 16-byte vectors)
+    const int nslices = (nvec + 127) / 128;
+    const int items = T * nslices;
+    for (int it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += nwarps) {
+        const int t = it / nslices;
+        const int v0 = (it - t * nslices) * 128;
         const int my_slot = lane < kk ? __ldg(slot_of + (size_t)t * kk + lane) : -1;
         const uint4* src = x + (size_t)t * nvec;
-        for (int v0 = 0; v0 < nvec; v0 += 32 * 4) {
+        {
             uint4 val[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -50,18 +55,24 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_fp8_kernel(
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int nvec = H / 8;     // 8 bf16 per 16-byte vector
     const int ngroups = H / kQG;
-    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    // work item = (token, slice of 128 vectors = 8 groups of 1x128), passes of 32
+    const int nslices = (nvec + 127) / 128;
+    const int items = T * nslices;
+    for (int it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += nwarps) {
+        const int t = it / nslices;
+        const int vbeg = (it - t * nslices) * 128;
+        const int vend = min(nvec, vbeg + 128);
         const int my_slot = lane < kk ? __ldg(slot_of + (size_t)t * kk + lane) : -1;
         const uint4* src = x + (size_t)t * nvec;
         // the row is read ahead one pass (two 16-byte loads a lane in flight)
-        uint4 next = lane < nvec ? __ldg(src + lane) : make_uint4(0u, 0u, 0u, 0u);
-        for (int v = lane; v - lane < nvec; v += 32) {
+        uint4 next = vbeg + lane < vend ? __ldg(src + vbeg + lane) : make_uint4(0u, 0u, 0u, 0u);
+        for (int v = vbeg + lane; v - lane < vend; v += 32) {
             // H is a multiple of 128, so a half-warp is either fully inside or fully out
-            const bool in = v < nvec;
+            const bool in = v < vend;
             float f[8];
             float amax = 0.0f;
             const uint4 raw = next;
-            if (v + 32 < nvec) next = __ldg(src + v + 32);
+            if (v + 32 < vend) next = __ldg(src + v + 32);
             if (in) {
                 const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -98,7 +109,9 @@ cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int
                             void* xe, float* xe_scale, int grid_cap, cudaStream_t st) {
     if (T <= 0) return cudaSuccess;
     const int kk = c.top_k + c.num_shared;
-    int grid = (T + 7) / 8;
+    const int nvec_io = c.hidden * io_bytes(c.dtype) / 16;
+    const long items = (long)T * ((nvec_io + 127) / 128);
+    int grid = (int)((items + 7) / 8);
     if (grid > grid_cap) grid = grid_cap;
     if (c.dtype == MOE_FP8_E4M3)
         return launch_pdl(dispatch_fp8_kernel, grid, kDispatchThreads, 0, st, T, kk, c.hidden,
