@@ -179,10 +179,12 @@ def launches_per_step(wl, split_two: bool) -> int:
 
 
 def ffn_source_hash() -> str:
+    """Hash of the device sources of the FFN kernels (a profile's DRAM counters apply
+    only while these are unchanged)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_dispatch_route_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("ffn") or name in ("common.cuh", "kernels.h", "tc_ptx.cuh"):
+        if name.startswith("ffn") or name in ("common.cuh", "tc_ptx.cuh"):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
     return h.hexdigest()[:16]
