@@ -166,15 +166,17 @@ def max_over_ranks(v: float, world: int) -> float:
 
 
 def launches_per_step(wl, split_two: bool) -> int:
-    """Kernels this library launches for one layer call (route, plan passes, dispatch,
-    the two FFN kernels, combine -- per ubatch)."""
+    """Kernels this library launches for one layer call, per ubatch: route; plan and
+    dispatch (one fused kernel when the plan is a single chunk); the two FFN kernels;
+    combine."""
     kk = wl.top_k + wl.num_shared
     tpc = max(1, 4096 // kk)
     sizes = [wl.split, wl.T - wl.split] if split_two else [wl.T]
     n = 0
     for Tu in sizes:
         chunks = max(1, math.ceil(Tu / tpc))
-        n += 1 + (2 if chunks > 1 else 1) + 1 + 2 + 1
+        # route, (plan + dispatch fused | plan count + plan assign + dispatch), 2 FFN kernels, combine
+        n += 1 + (1 if chunks == 1 else 3) + 2 + 1
     return n
 
 

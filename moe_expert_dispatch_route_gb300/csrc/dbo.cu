@@ -281,10 +281,17 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
             case MOE_OP_WAIT: ce = cudaStreamWaitEvent(q, h->ev[op.ev], 0); break;
             case MOE_OP_ROUTE: ce = launch_route(c, Tu, logits_u, a->bias, ids_u, w_u, comm_grid, q); break;
             case MOE_OP_PLAN:
-                ce = launch_plan(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, nullptr, err,
-                                 reinterpret_cast<int32_t*>(b + L.hist), comm_grid, q);
+                if (plan_dispatch_fusable(c, Tu)) {  // small batch: plan and dispatch in one launch
+                    const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
+                    ce = launch_plan_dispatch(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, err, xu, xe,
+                                              xe_scale, comm_grid, q);
+                } else {
+                    ce = launch_plan(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, nullptr, err,
+                                     reinterpret_cast<int32_t*>(b + L.hist), comm_grid, q);
+                }
                 break;
             case MOE_OP_DISPATCH: {
+                if (plan_dispatch_fusable(c, Tu)) break;  // done with the plan
                 const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
                 ce = launch_dispatch(c, Tu, xu, slot_of, xe, xe_scale, comm_grid, q);
                 break;
@@ -430,10 +437,16 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
                 ce = launch_route(c, Tu, a->logits[l] + (size_t)t0[u] * c.num_experts, a->bias, ids, wts, comm_grid, q);
                 break;
             case MOE_OP_PLAN:
-                ce = launch_plan(c, Tu, ids, capacity, align, counts, offsets, slot_of, nullptr, err,
-                                 reinterpret_cast<int32_t*>(b + U.hist), comm_grid, q);
+                if (plan_dispatch_fusable(c, Tu))
+                    ce = launch_plan_dispatch(c, Tu, ids, capacity, align, counts, offsets, slot_of, err, act, xe,
+                                              xe_scale, comm_grid, q);
+                else
+                    ce = launch_plan(c, Tu, ids, capacity, align, counts, offsets, slot_of, nullptr, err,
+                                     reinterpret_cast<int32_t*>(b + U.hist), comm_grid, q);
                 break;
-            case MOE_OP_DISPATCH: ce = launch_dispatch(c, Tu, act, slot_of, xe, xe_scale, comm_grid, q); break;
+            case MOE_OP_DISPATCH:
+                if (!plan_dispatch_fusable(c, Tu)) ce = launch_dispatch(c, Tu, act, slot_of, xe, xe_scale, comm_grid, q);
+                break;
             case MOE_OP_FFN: {
                 FfnArgs fa{counts, offsets, U.rows, xe, xe_scale, a->w13[l], fp8 ? a->w13_scale[l] : nullptr, a->w2[l],
                            fp8 ? a->w2_scale[l] : nullptr, ye, b + U.ffn, err, two && u == 1 ? 1 : 0};
