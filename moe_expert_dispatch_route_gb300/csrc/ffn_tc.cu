@@ -40,11 +40,35 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;  // full, empty, tmem full, tmem empty, drain
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kNumBars * 8 + 16 +
-                              3 * (kMaxExperts + 1) * sizeof(int) + 512 * sizeof(float) + 256 * sizeof(int);
-constexpr int kF8Threads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 promotion + epilogue
-constexpr int kF8BK = 128;       // e4m3 elements per k-block = one 128-wide scale block
+constexpr int kF8BK = 128;  // e4m3 elements per k-block = one 128-wide scale block
+
+// FP8 tile geometry.  up: 128 x 256 tiles (gate 128 | up 128 columns, so that a whole
+// 1x128 group of h is formed in one tile), one accumulator, 4 stages of 48 KB.  down:
+// 128 x 128 tiles, two accumulators (the epilogue of one tile overlaps the next tile's
+// MMAs), 6 stages of 32 KB.  Scale factors of each stage are staged in shared memory
+// (kSfStageBytes) and copied into TMEM slot kSfCol + 16 * stage.
+template <bool kUp>
+struct F8 {
+    static constexpr int N = kUp ? 256 : 128;
+    static constexpr int AccBufs = kUp ? 1 : 2;
+    static constexpr int Stages = kUp ? 4 : 6;
+    static constexpr int StageBytes = kBM * kF8BK + N * kF8BK;
+};
+constexpr int kSfCol = 256;
+constexpr int kSfStageBytes = 1536;  // A scales, B scales of rows 0-127, of rows 128-255 (512 B each)
+constexpr int kMaxStages = 6;
+constexpr int kNumBars = 2 * kMaxStages + 2 + 2 + 1;  // full, empty, tmem full, tmem empty, drain
+constexpr size_t kSmemTail =
+    kNumBars * 8 + 16 + 3 * (kMaxExperts + 1) * sizeof(int) + 512 * sizeof(float) + 256 * sizeof(int);
+constexpr size_t smem_bytes(int stages, int stage_bytes, int sf_bytes) {
+    return 1024 + (size_t)stages * (stage_bytes + sf_bytes) + kSmemTail;
+}
+constexpr size_t kSmemBytes = smem_bytes(kStages, kStageBytes, 0);
+template <bool kUp>
+constexpr size_t kF8SmemBytes = smem_bytes(F8<kUp>::Stages, F8<kUp>::StageBytes, kSfStageBytes);
+constexpr int kF8Threads = 352;  // warp 0 TMA, warp 1 MMA, warp 2 scale staging, warps 3..10 epilogue
+constexpr int kF8FirstEpiWarp = 3;
+constexpr int kScGroup = 8;      // fp8: k-blocks of scales loaded at once
 
 // A tiles are loaded with the smallest box of 16 / 32 / 64 / 128 rows that covers the
 // tile's rows: at decode an expert has a handful of rows, and fetching 128 would
@@ -76,6 +100,7 @@ struct TcParams {
 
 struct Smem {
     uint8_t* stages;
+    uint8_t* sf;  // fp8: per stage, the scale factors staged for tcgen05.cp
     uint64_t* full;
     uint64_t* empty;
     uint64_t* tfull;
@@ -90,14 +115,16 @@ struct Smem {
     volatile int* xseq;  // [2 halves][128 rows] tile sequence number of the value
 };
 
-__device__ __forceinline__ Smem carve(uint8_t* raw) {
+__device__ __forceinline__ Smem carve(uint8_t* raw, int stages, int stage_bytes, int sf_bytes) {
     Smem s;
     uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.stages = p;
-    p += (size_t)kStages * kStageBytes;
+    p += (size_t)stages * stage_bytes;
+    s.sf = p;
+    p += (size_t)stages * sf_bytes;
     s.full = reinterpret_cast<uint64_t*>(p);
-    s.empty = s.full + kStages;
-    s.tfull = s.empty + kStages;
+    s.empty = s.full + stages;
+    s.tfull = s.empty + stages;
     s.tempty = s.tfull + 2;
     s.drain = s.tempty + 2;
     s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 1);
@@ -360,7 +387,7 @@ __device__ void epilogue(const TcParams& p, const Smem& s, int total, uint32_t t
 template <bool kUp>
 __global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const Smem s = carve(smem_raw);
+    const Smem s = carve(smem_raw, kStages, kStageBytes, 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -410,46 +437,186 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_c
 
 // ---------------------------------------------------------------- FP8 (e4m3) kernels
 //
-// Same tiles and TMA ring as the bf16 kernels, with k-blocks of 128 e4m3 elements (one
-// 128-byte row), which is exactly one 128-wide scale block.  Each k-block's four
-// kind::f8f6f4 MMAs (K = 32) write a fresh partial product into one of two TMEM
-// buffers; eight promotion warps read it back, multiply by a_scale[row][kb] *
-// b_scale[n-block][kb] (both powers of two) and accumulate in fp32 registers (each
-// thread: one row, 128 of the 256 columns), while the MMAs of the next k-block fill
-// the other buffer.  The up kernel's epilogue forms h = silu(g) * u, finds the 1x128
-// group amax of its row with its partner thread (the other half of the columns)
-// through shared memory, and stores h as e4m3 with its power-of-two scale; the down
-// kernel stores ye as bf16.
+// Same persistent tile loop and TMA ring as the bf16 kernels, with k-blocks of 128
+// e4m3 elements (one 128-byte row), which is exactly one 128-wide scale block.  The
+// scales are powers of two, so they are exact UE8M0 scale factors and the tensor core
+// applies them itself: per k-block, four kind::mxf8f6f4 MMAs (K = 32) accumulate
+// (A * a_scale[row][kb]) . (B * b_scale[n-block][kb])^T straight into a TMEM
+// accumulator.  A staging warp writes each k-block's scale factors into shared memory
+// next to the stage's operand tiles (the TMA producer only issues copies); the MMA
+// thread copies them into the stage's TMEM scale slot (tcgen05.cp) right before the
+// stage's MMAs, which execute in order after it.
+// Epilogues: up forms h = silu(g) * u, finds the 1x128 group amax of its row with its
+// partner thread (the other half of the columns) through shared memory and stores h
+// as e4m3 with its power-of-two scale; down stores ye as bf16.  The up kernel's single
+// accumulator is moved into registers and released before any of that arithmetic.
 
-__device__ void mma_issuer_f8(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
+__device__ __forceinline__ uint32_t ue8m0x4(float pow2) {  // the biased exponent, in all four bytes
+    const uint32_t e = (__float_as_uint(pow2) >> 23) & 0xffu;
+    return e * 0x01010101u;
+}
+
+// One thread: the stage's TMA loads (A box and one or two 128-row B boxes).
+template <bool kUp>
+__device__ void producer_f8(const TcParams& p, const Smem& s, int total) {
+    using G = F8<kUp>;
     int stage = 0;
     uint32_t phase = 0;
-    int pb = 0;
-    uint32_t pph = 0;
+    uint32_t pending = 0, pend_par = 0;
     bool ok = true;
-    constexpr uint32_t idesc = tc::idesc_e4m3_f32(kBM, kBN);
     for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
+        const Tile t = decode_tile(p, s, total, lin);
+        const int b0 = t.e * p.NB + t.nt * 128;
+        const int b1 = t.e * p.NB + p.I + t.nt * 128;  // up kernel: the up rows
+        int abox = 0;
+        while (abox < kNumABoxes - 1 && a_box_rows(abox) < t.rows) ++abox;
+        const uint32_t tx = (uint32_t)(a_box_rows(abox) * kF8BK + G::N * kF8BK);
         for (int kb = 0; kb < p.kblocks; ++kb) {
-            if (!tc::mbar_wait(&s.tempty[pb], pph ^ 1u, s.abort) || !tc::mbar_wait(&s.full[stage], phase, s.abort)) {
+            if (!tc::mbar_wait(&s.empty[stage], phase ^ 1u, s.abort)) {
+                ok = false;
+                break;
+            }
+            uint8_t* a = s.stages + (size_t)stage * G::StageBytes;
+            uint8_t* b = a + kBM * kF8BK;
+            tc::mbar_arrive_expect_tx(&s.full[stage], tx);
+            tc::tma_load_2d(a, &p.tmA[abox], &s.full[stage], kb * kF8BK, t.row0);
+            tc::tma_load_2d(b, &p.tmB, &s.full[stage], kb * kF8BK, b0);
+            if (kUp) tc::tma_load_2d(b + 128 * kF8BK, &p.tmB, &s.full[stage], kb * kF8BK, b1);
+            pending |= 1u << stage;
+            pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == G::Stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        fail(s, p.err);
+        // let the copies already issued land before the CTA exits
+        for (int st = 0; st < G::Stages; ++st)
+            if ((pending >> st) & 1u) {
+                const uint64_t t0 = tc::globaltimer();
+                while (!tc::mbar_try_wait(&s.full[st], (pend_par >> st) & 1u) &&
+                       tc::globaltimer() - t0 < tc::kWaitTimeoutNs) {
+                }
+            }
+    }
+}
+
+// Whole warp: for each stage, its row of the stage's three 32 x 16-byte scale blocks:
+// A (word c of row i = the scale of tile row 32c + i, the layout the MMA reads after
+// the replicating copy), B rows 0-127 and B rows 128-255 (one value each), then the
+// second arrival on full[stage].  Scales are loaded kScGroup k-blocks ahead.
+template <bool kUp>
+__device__ void scale_stager_f8(const TcParams& p, const Smem& s, int total) {
+    using G = F8<kUp>;
+    const int lane = threadIdx.x & 31;
+    const int ksb = p.K / kF8BK;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
+        const Tile t = decode_tile(p, s, total, lin);
+        const float* arow[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int rr = 32 * c + lane;
+            const int64_t row = (int64_t)t.row0 + rr;
+            arow[c] = (rr < t.rows && row < p.max_rows) ? p.a_scale + row * ksb : nullptr;
+        }
+        const float* bsc = p.b_scale + (size_t)t.e * (p.NB / kF8BK) * ksb;
+        const float* bs0 = bsc + (size_t)t.nt * ksb;
+        const float* bs1 = bsc + (size_t)(p.I / kF8BK + t.nt) * ksb;  // up kernel only
+        float ca[kScGroup][4], c0[kScGroup], c1[kScGroup];
+        auto load = [&](int kb0, float (&va)[kScGroup][4], float (&v0)[kScGroup], float (&v1)[kScGroup]) {
+#pragma unroll
+            for (int j = 0; j < kScGroup; ++j) {
+                const int kb = kb0 + j;
+                const bool in = kb < p.kblocks;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) va[j][c] = (in && arow[c]) ? __ldg(arow[c] + kb) : 1.0f;
+                v0[j] = in ? __ldg(bs0 + kb) : 1.0f;
+                v1[j] = (in && kUp) ? __ldg(bs1 + kb) : 1.0f;
+            }
+        };
+        load(0, ca, c0, c1);
+        for (int kb0 = 0; kb0 < p.kblocks && ok; kb0 += kScGroup) {
+            float na[kScGroup][4], n0[kScGroup], n1[kScGroup];
+            load(kb0 + kScGroup, na, n0, n1);
+#pragma unroll
+            for (int j = 0; j < kScGroup; ++j) {
+                if (kb0 + j >= p.kblocks) break;
+                if (!tc::mbar_wait(&s.empty[stage], phase ^ 1u, s.abort)) {
+                    ok = false;
+                    break;
+                }
+                uint4* sf = reinterpret_cast<uint4*>(s.sf + (size_t)stage * kSfStageBytes);
+                sf[lane] = make_uint4(ue8m0x4(ca[j][0]), ue8m0x4(ca[j][1]), ue8m0x4(ca[j][2]), ue8m0x4(ca[j][3]));
+                const uint32_t w0 = ue8m0x4(c0[j]), w1 = ue8m0x4(c1[j]);
+                sf[32 + lane] = make_uint4(w0, w0, w0, w0);
+                if (kUp) sf[64 + lane] = make_uint4(w1, w1, w1, w1);
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&s.full[stage]);
+                if (++stage == G::Stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kScGroup; ++j) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ca[j][c] = na[j][c];
+                c0[j] = n0[j];
+                c1[j] = n1[j];
+            }
+        }
+    }
+    if (!ok) fail(s, p.err);
+}
+
+template <bool kUp>
+__device__ void mma_issuer_f8(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
+    using G = F8<kUp>;
+    int stage = 0, buf = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    constexpr uint32_t idesc = tc::idesc_mx_e4m3(kBM, G::N);
+    for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
+        if (!tc::mbar_wait(&s.tempty[buf], acc_phase ^ 1u, s.abort)) {
+            ok = false;
+            break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * G::N);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (!tc::mbar_wait(&s.full[stage], phase, s.abort)) {
                 ok = false;
                 break;
             }
             tc::tc_fence_after();
-            const uint32_t d = tmem_base + (uint32_t)(pb * kBN);
-            const uint32_t a_addr = tc::smem_u32(s.stages + (size_t)stage * kStageBytes);
-            const uint32_t b_addr = a_addr + kABytes;
+            const uint32_t a_addr = tc::smem_u32(s.stages + (size_t)stage * G::StageBytes);
+            const uint32_t b_addr = a_addr + kBM * kF8BK;
+            const uint32_t sf_smem = tc::smem_u32(s.sf + (size_t)stage * kSfStageBytes);
+            const uint32_t sf = tmem_base + (uint32_t)(kSfCol + 16 * stage);
+            tc::tmem_cp_32x128b_x4(sf, tc::desc_rows16(sf_smem));                // A: columns sf .. sf+3
+            tc::tmem_cp_32x128b_x4(sf + 8, tc::desc_rows16(sf_smem + 512));       // B rows 0-127
+            if (kUp) tc::tmem_cp_32x128b_x4(sf + 12, tc::desc_rows16(sf_smem + 1024));  // B rows 128-255
 #pragma unroll
             for (int kk = 0; kk < kF8BK / 32; ++kk)
-                tc::mma_e4m3(d, tc::desc_sw128_kmajor(a_addr + kk * 32), tc::desc_sw128_kmajor(b_addr + kk * 32),
-                             idesc, kk != 0 ? 1u : 0u);
-            tc::mma_commit(&s.empty[stage]);
-            tc::mma_commit(&s.tfull[pb]);
-            if (++stage == kStages) {
+                tc::mma_mx_e4m3(d, tc::desc_sw128_kmajor(a_addr + kk * 32), tc::desc_sw128_kmajor(b_addr + kk * 32),
+                                idesc, sf, sf + 8, (kb | kk) != 0 ? 1u : 0u);
+            tc::mma_commit(&s.empty[stage]);  // stage (tiles and scales) free once these finish
+            if (++stage == G::Stages) {
                 stage = 0;
                 phase ^= 1u;
             }
-            pb ^= 1;
-            if (pb == 0) pph ^= 1u;
+        }
+        if (!ok) break;
+        tc::mma_commit(&s.tfull[buf]);
+        if (++buf == G::AccBufs) {
+            buf = 0;
+            acc_phase ^= 1u;
         }
     }
     if (!ok) fail(s, p.err);
@@ -459,95 +626,58 @@ __device__ void mma_issuer_f8(const TcParams& p, const Smem& s, int total, uint3
     }
 }
 
-// acc += partial * sc for 32 columns of this thread's TMEM lane, as packed two-wide
-// fp32 FMAs (acc[i] holds columns 2i, 2i+1).  Loaded 16 columns at a time: with 10
-// warps per SM a thread has at most 168 registers, 128 of which are accumulators.
-__device__ __forceinline__ void promote32(uint32_t taddr, float sc, float2* acc) {
-    const float2 s2 = make_float2(sc, sc);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t v[16];
-        tc::tmem_ld16(taddr + 16 * h, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            acc[8 * h + i] =
-                __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), s2, acc[8 * h + i]);
-    }
+__device__ __forceinline__ void release_acc(const Smem& s, int buf) {
+    tc::tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&s.tempty[buf]);
 }
 
+// Eight warps, two per TMEM lane quarter; `half` selects half of the tile's columns.
 template <bool kUp>
 __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
+    using G = F8<kUp>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q = warp & 3;           // TMEM lane quarter
-    const int half = (warp - 2) >> 2;  // which half of the 256 columns
+    const int q = warp & 3;
+    const int half = (warp - kF8FirstEpiWarp) >> 2;
     const int r = q * 32 + lane;
-    const int ksb = p.K / kF8BK;      // scale blocks along K
-    int pb = 0;
-    uint32_t pph = 0;
+    int buf = 0;
+    uint32_t acc_phase = 0;
     int seq = 0;
     bool ok = true;
     for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
         const Tile t = decode_tile(p, s, total, lin);
         const int64_t row = (int64_t)t.row0 + r;
-        const bool in_rows = row < p.max_rows;
-        const float* asc = p.a_scale + (in_rows ? row : 0) * ksb;
-        const float* bsc = p.b_scale + (size_t)t.e * (p.NB / kF8BK) * ksb;
-        const int nb0 = kUp ? t.nt : 2 * t.nt + half;  // gate (up kernel) or output block
-        const int nb1 = kUp ? p.I / kF8BK + t.nt : nb0;  // up block (up kernel)
-        float2 acc[64];  // up: gate columns in acc[0..31], up columns in acc[32..63]
-#pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.0f, 0.0f);
-        // a warp whose 32 rows are all past the tile's rows has nothing to promote (at
+        const bool valid = r < t.rows;
+        // a warp whose 32 rows are all past the tile's rows has nothing to read (at
         // decode most tiles hold fewer than 32 rows)
         const bool busy = q * 32 < t.rows;
-        const float* bs0 = bsc + (size_t)nb0 * ksb;
-        const float* bs1 = bsc + (size_t)nb1 * ksb;
-        // scales of the next k-block are loaded while the current one is promoted
-        float sa_n = (busy && in_rows) ? __ldg(asc) : 0.0f;
-        float sb0_n = busy ? __ldg(bs0) : 0.0f;
-        float sb1_n = (busy && kUp) ? __ldg(bs1) : 0.0f;
-        for (int kb = 0; kb < p.kblocks; ++kb) {
-            const float s0 = sa_n * sb0_n, s1 = sa_n * sb1_n;
-            if (busy && kb + 1 < p.kblocks) {
-                sa_n = in_rows ? __ldg(asc + kb + 1) : 0.0f;
-                sb0_n = __ldg(bs0 + kb + 1);
-                if (kUp) sb1_n = __ldg(bs1 + kb + 1);
-            }
-            if (!tc::mbar_wait(&s.tfull[pb], pph, s.abort)) {
-                ok = false;
-                break;
-            }
-            tc::tc_fence_after();
-            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(pb * kBN);
-            if (busy) {
-                if (kUp) {
-                    promote32(tb + 64 * half, s0, acc);
-                    promote32(tb + 64 * half + 32, s0, acc + 16);
-                    promote32(tb + 128 + 64 * half, s1, acc + 32);
-                    promote32(tb + 128 + 64 * half + 32, s1, acc + 48);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) promote32(tb + 128 * half + 32 * c, s0, acc + 16 * c);
-                }
-            }
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&s.tempty[pb]);
-            pb ^= 1;
-            if (pb == 0) pph ^= 1u;
+        if (!tc::mbar_wait(&s.tfull[buf], acc_phase, s.abort)) {
+            ok = false;
+            break;
         }
-        if (!ok) break;
-        const bool valid = r < t.rows;
+        tc::tc_fence_after();
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * G::N);
         if (kUp) {
-            // h for this thread's 64 columns (written over the gate pairs)
+            uint32_t g0[32], g1[32], u0[32], u1[32];  // gate / up columns 64*half .. +63
+            if (busy) {
+                tc::tmem_ld32(tb + 64 * half, g0);
+                tc::tmem_ld32(tb + 64 * half + 32, g1);
+                tc::tmem_ld32(tb + 128 + 64 * half, u0);
+                tc::tmem_ld32(tb + 128 + 64 * half + 32, u1);
+                tc::tmem_wait_ld();
+            }
+            release_acc(s, buf);
             float amax = 0.0f;
+            if (busy) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float g0 = acc[i].x, g1 = acc[i].y;
-                acc[i].x = g0 / (1.0f + expf(-g0)) * acc[32 + i].x;
-                acc[i].y = g1 / (1.0f + expf(-g1)) * acc[32 + i].y;
-                amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
+                for (int i = 0; i < 32; ++i) {
+                    const float ga = __uint_as_float(g0[i]), gb = __uint_as_float(g1[i]);
+                    const float ha = ga / (1.0f + expf(-ga)) * __uint_as_float(u0[i]);
+                    const float hb = gb / (1.0f + expf(-gb)) * __uint_as_float(u1[i]);
+                    g0[i] = __float_as_uint(ha);
+                    g1[i] = __float_as_uint(hb);
+                    amax = fmaxf(amax, fmaxf(fabsf(ha), fabsf(hb)));
+                }
             }
             // the row's other 64 columns belong to the partner thread: exchange amax
             ++seq;
@@ -565,13 +695,16 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
             if (!ok) break;
             __threadfence_block();
             amax = fmaxf(amax, s.xval[(par * 2 + 1 - half) * 128 + r]);
-            const int se = fp8_scale_exp(amax);
             if (valid) {
+                const int se = fp8_scale_exp(amax);
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const uint16_t lo = f2_to_e4m3x2(scalbnf(acc[2 * i].x, -se), scalbnf(acc[2 * i].y, -se));
-                    const uint16_t hi = f2_to_e4m3x2(scalbnf(acc[2 * i + 1].x, -se), scalbnf(acc[2 * i + 1].y, -se));
+                    const uint32_t* src = i < 8 ? g0 + 4 * i : g1 + 4 * (i - 8);
+                    const uint16_t lo = f2_to_e4m3x2(scalbnf(__uint_as_float(src[0]), -se),
+                                                     scalbnf(__uint_as_float(src[1]), -se));
+                    const uint16_t hi = f2_to_e4m3x2(scalbnf(__uint_as_float(src[2]), -se),
+                                                     scalbnf(__uint_as_float(src[3]), -se));
                     w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + row * p.I + t.nt * 128 + 64 * half);
@@ -579,13 +712,34 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
                 for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                 if (half == 0) p.out_scale[row * (p.I / kF8BK) + t.nt] = scalbnf(1.0f, se);
             }
-        } else if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.H + t.nt * kBN + 128 * half);
+        } else {
+            uint32_t a0[32], a1[32];  // columns 64*half .. +63 of the 128-wide tile
+            if (busy) {
+                tc::tmem_ld32(tb + 64 * half, a0);
+                tc::tmem_ld32(tb + 64 * half + 32, a1);
+                tc::tmem_wait_ld();
+            }
+            release_acc(s, buf);
+            if (valid) {
+                uint4* dst =
+                    reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.H + t.nt * G::N + 64 * half);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                dst[i] = make_uint4(pack_bf16x2(acc[4 * i].x, acc[4 * i].y), pack_bf16x2(acc[4 * i + 1].x, acc[4 * i + 1].y),
-                                    pack_bf16x2(acc[4 * i + 2].x, acc[4 * i + 2].y),
-                                    pack_bf16x2(acc[4 * i + 3].x, acc[4 * i + 3].y));
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pack_bf16x2(__uint_as_float(a0[8 * i]), __uint_as_float(a0[8 * i + 1])),
+                                        pack_bf16x2(__uint_as_float(a0[8 * i + 2]), __uint_as_float(a0[8 * i + 3])),
+                                        pack_bf16x2(__uint_as_float(a0[8 * i + 4]), __uint_as_float(a0[8 * i + 5])),
+                                        pack_bf16x2(__uint_as_float(a0[8 * i + 6]), __uint_as_float(a0[8 * i + 7])));
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[4 + i] = make_uint4(pack_bf16x2(__uint_as_float(a1[8 * i]), __uint_as_float(a1[8 * i + 1])),
+                                            pack_bf16x2(__uint_as_float(a1[8 * i + 2]), __uint_as_float(a1[8 * i + 3])),
+                                            pack_bf16x2(__uint_as_float(a1[8 * i + 4]), __uint_as_float(a1[8 * i + 5])),
+                                            pack_bf16x2(__uint_as_float(a1[8 * i + 6]), __uint_as_float(a1[8 * i + 7])));
+            }
+        }
+        if (++buf == G::AccBufs) {
+            buf = 0;
+            acc_phase ^= 1u;
         }
     }
     if (!ok) fail(s, p.err);
@@ -593,15 +747,16 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
 
 template <bool kUp>
 __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_constant__ TcParams p) {
+    using G = F8<kUp>;
     extern __shared__ uint8_t smem_raw[];
-    const Smem s = carve(smem_raw);
+    const Smem s = carve(smem_raw, G::Stages, G::StageBytes, kSfStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            tc::mbar_init(&s.full[i], 1);
+        for (int i = 0; i < G::Stages; ++i) {
+            tc::mbar_init(&s.full[i], 2);
             tc::mbar_init(&s.empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < G::AccBufs; ++i) {
             tc::mbar_init(&s.tfull[i], 1);
             tc::mbar_init(&s.tempty[i], 8);
         }
@@ -626,9 +781,11 @@ __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_
     const int total = s.tstart[p.NE];
 
     if (warp == 0) {
-        if (lane == 0) producer<kUp, kF8BK>(p, s, total);
+        if (lane == 0) producer_f8<kUp>(p, s, total);
     } else if (warp == 1) {
-        if (lane == 0) mma_issuer_f8(p, s, total, tmem_base);
+        if (lane == 0) mma_issuer_f8<kUp>(p, s, total, tmem_base);
+    } else if (warp == 2) {
+        scale_stager_f8<kUp>(p, s, total);
     } else {
         epilogue_f8<kUp>(p, s, total, tmem_base);
     }
@@ -674,8 +831,9 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
     static int configured_dev = -1;
     const int dev = device_info().device;
     auto kern = kFp8 ? ffn_tc_fp8_kernel<kUp> : ffn_tc_bf16_kernel<kUp>;
+    const size_t smem = kFp8 ? kF8SmemBytes<kUp> : kSmemBytes;
     if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
@@ -685,7 +843,7 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kFp8 ? kF8Threads : kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -699,8 +857,11 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
 
 bool ffn_tc_supported(const moe_config& c) {
     const DeviceInfo& d = device_info();
+    const size_t smem = c.dtype == MOE_FP8_E4M3 ? (kF8SmemBytes<true> > kF8SmemBytes<false> ? kF8SmemBytes<true>
+                                                                                              : kF8SmemBytes<false>)
+                                                : kSmemBytes;
     return (c.dtype == MOE_BF16 || c.dtype == MOE_FP8_E4M3) && d.cc_major == 10 && c.hidden % kBN == 0 &&
-           c.inter % 128 == 0 && d.smem_optin >= kSmemBytes && encode_fn() != nullptr;
+           c.inter % 128 == 0 && d.smem_optin >= smem && encode_fn() != nullptr;
 }
 
 cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st) {
@@ -743,7 +904,7 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     dn.K = I;
     dn.kblocks = I / kelems;
     dn.NB = H;
-    dn.ntn = H / kBN;
+    dn.ntn = H / (fp8 ? F8<false>::N : kBN);
     dn.out = a.ye;
     dn.a_scale = h_scale;
     dn.b_scale = a.w2_scale;

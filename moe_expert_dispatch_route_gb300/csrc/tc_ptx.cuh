@@ -1,6 +1,7 @@
 // Inline-PTX wrappers for the Blackwell (sm_100-family, here sm_103a) tensor-core
 // path: mbarriers with bounded waits, TMA tile loads, TMEM allocation, tcgen05.mma
-// and tcgen05.ld.  Written from the PTX ISA's descriptions of these instructions.
+// (dense bf16 and block-scaled e4m3), tcgen05.cp and tcgen05.ld.  Written from the PTX
+// ISA's descriptions of these instructions.
 #pragma once
 
 #include <cuda.h>
@@ -134,20 +135,28 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format 0), fp32
-// accumulator, both operands K-major, dense.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::mxf8f6f4 (block-scaled, fp32 accumulator) with e4m3
+// A and B (format 0), both K-major, dense, UE8M0 scale factors (bit 23), scale-factor
+// byte 0 of both scale columns (B id in [4,6), A id in [29,31)), N >> 3 in [17,23),
+// M >> 4 in [24,29).
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N) {
+    return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T with e4m3 operands (K = 32 per instruction).
-__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+// D[tmem] (+)= (A[smem] * sfa) * (B[smem] * sfb)^T with e4m3 operands (K = 32 per
+// instruction) and one UE8M0 scale per row of A and per row of B for these 32 K
+// elements.  Scale layout in TMEM (measured on the device): the scale of A row m sits
+// in lane m, column sfa + m/32; the scale of B row n in lane 32q + n%32 of every lane
+// quarter q, column sfb + n/32; the byte within the 32-bit cell is the descriptor's
+// scale-factor id (0 here).
+__device__ __forceinline__ void mma_mx_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
 
@@ -184,18 +193,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
-// This thread's TMEM lane, 16 consecutive 32-bit columns starting at taddr.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15])
-        : "r"(taddr));
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory descriptor of a plain (unswizzled) block of 16-byte rows stored one
+// after another: 8-row core matrices 128 bytes apart (stride byte offset), a single
+// 16-byte column (the leading byte offset is not used and set to the same 128).
+__device__ __forceinline__ uint64_t desc_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(128 >> 4) << 16;
+    d |= (uint64_t)(128 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
 }
 
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Copies 32 rows x 128 bits of shared memory (desc_rows16) into TMEM columns
+// taddr .. taddr+3, replicated into all four lane quarters: row i lands in lane
+// 32q + i of every quarter q.  Issued by one thread; executes in order with the
+// tcgen05.mma instructions this thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Makes this thread's generic-proxy writes to shared memory visible to the async proxy
+// (TMA, tcgen05.cp, tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 }  // namespace tc
 }  // namespace moe
