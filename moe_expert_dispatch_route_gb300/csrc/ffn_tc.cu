@@ -503,73 +503,99 @@ __device__ void producer_f8(const TcParams& p, const Smem& s, int total) {
     }
 }
 
+// Position of the scale stager's loads in the CTA's sequence of (tile, k-block) steps,
+// with the tile's scale rows for this lane.
+struct ScaleCursor {
+    int lin, kb;
+    const float* arow[4];  // A scale rows of tile rows 32c + lane (null past the tile)
+    const float* bs0;      // B scales of the tile's first 128 weight rows
+    const float* bs1;      // up kernel: of the up rows
+};
+
+template <bool kUp>
+__device__ __forceinline__ void cursor_tile(const TcParams& p, const Smem& s, int total, ScaleCursor& c) {
+    const int lane = threadIdx.x & 31;
+    const int ksb = p.K / kF8BK;
+    c.kb = 0;
+    if (c.lin >= total) return;
+    const Tile t = decode_tile(p, s, total, c.lin);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int rr = 32 * i + lane;
+        const int64_t row = (int64_t)t.row0 + rr;
+        c.arow[i] = (rr < t.rows && row < p.max_rows) ? p.a_scale + row * ksb : nullptr;
+    }
+    const float* bsc = p.b_scale + (size_t)t.e * (p.NB / kF8BK) * ksb;
+    c.bs0 = bsc + (size_t)t.nt * ksb;
+    c.bs1 = bsc + (size_t)(p.I / kF8BK + t.nt) * ksb;
+}
+
+// Loads the scales of the cursor's step (1.0 past the end) and advances it.
+template <bool kUp>
+__device__ __forceinline__ void cursor_fetch(const TcParams& p, const Smem& s, int total, ScaleCursor& c,
+                                             float (&va)[4], float& v0, float& v1) {
+    const bool in = c.lin < total;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) va[i] = (in && c.arow[i]) ? __ldg(c.arow[i] + c.kb) : 1.0f;
+    v0 = in ? __ldg(c.bs0 + c.kb) : 1.0f;
+    v1 = (in && kUp) ? __ldg(c.bs1 + c.kb) : 1.0f;
+    if (in && ++c.kb == p.kblocks) {
+        c.lin += gridDim.x;
+        cursor_tile<kUp>(p, s, total, c);
+    }
+}
+
 // Whole warp: for each stage, its row of the stage's three 32 x 16-byte scale blocks:
 // A (word c of row i = the scale of tile row 32c + i, the layout the MMA reads after
 // the replicating copy), B rows 0-127 and B rows 128-255 (one value each), then the
-// second arrival on full[stage].  Scales are loaded kScGroup k-blocks ahead.
+// second arrival on full[stage].  The CTA's (tile, k-block) steps form one sequence;
+// scales are loaded kScGroup steps ahead of their use, across tile boundaries, so a
+// load's latency stays hidden even for tiles of a few k-blocks.
 template <bool kUp>
 __device__ void scale_stager_f8(const TcParams& p, const Smem& s, int total) {
     using G = F8<kUp>;
     const int lane = threadIdx.x & 31;
-    const int ksb = p.K / kF8BK;
+    const int tiles = blockIdx.x < (unsigned)total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int64_t steps = (int64_t)tiles * p.kblocks;
+    ScaleCursor cur;
+    cur.lin = blockIdx.x;
+    cursor_tile<kUp>(p, s, total, cur);
+    float ca[kScGroup][4], c0[kScGroup], c1[kScGroup];
+#pragma unroll
+    for (int j = 0; j < kScGroup; ++j) cursor_fetch<kUp>(p, s, total, cur, ca[j], c0[j], c1[j]);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
-        const Tile t = decode_tile(p, s, total, lin);
-        const float* arow[4];
+    for (int64_t step0 = 0; step0 < steps && ok; step0 += kScGroup) {
+        float na[kScGroup][4], n0[kScGroup], n1[kScGroup];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int rr = 32 * c + lane;
-            const int64_t row = (int64_t)t.row0 + rr;
-            arow[c] = (rr < t.rows && row < p.max_rows) ? p.a_scale + row * ksb : nullptr;
+        for (int j = 0; j < kScGroup; ++j) cursor_fetch<kUp>(p, s, total, cur, na[j], n0[j], n1[j]);
+#pragma unroll
+        for (int j = 0; j < kScGroup; ++j) {
+            if (step0 + j >= steps) break;
+            if (!tc::mbar_wait(&s.empty[stage], phase ^ 1u, s.abort)) {
+                ok = false;
+                break;
+            }
+            uint4* sf = reinterpret_cast<uint4*>(s.sf + (size_t)stage * kSfStageBytes);
+            sf[lane] = make_uint4(ue8m0x4(ca[j][0]), ue8m0x4(ca[j][1]), ue8m0x4(ca[j][2]), ue8m0x4(ca[j][3]));
+            const uint32_t w0 = ue8m0x4(c0[j]), w1 = ue8m0x4(c1[j]);
+            sf[32 + lane] = make_uint4(w0, w0, w0, w0);
+            if (kUp) sf[64 + lane] = make_uint4(w1, w1, w1, w1);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&s.full[stage]);
+            if (++stage == G::Stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
         }
-        const float* bsc = p.b_scale + (size_t)t.e * (p.NB / kF8BK) * ksb;
-        const float* bs0 = bsc + (size_t)t.nt * ksb;
-        const float* bs1 = bsc + (size_t)(p.I / kF8BK + t.nt) * ksb;  // up kernel only
-        float ca[kScGroup][4], c0[kScGroup], c1[kScGroup];
-        auto load = [&](int kb0, float (&va)[kScGroup][4], float (&v0)[kScGroup], float (&v1)[kScGroup]) {
 #pragma unroll
-            for (int j = 0; j < kScGroup; ++j) {
-                const int kb = kb0 + j;
-                const bool in = kb < p.kblocks;
+        for (int j = 0; j < kScGroup; ++j) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) va[j][c] = (in && arow[c]) ? __ldg(arow[c] + kb) : 1.0f;
-                v0[j] = in ? __ldg(bs0 + kb) : 1.0f;
-                v1[j] = (in && kUp) ? __ldg(bs1 + kb) : 1.0f;
-            }
-        };
-        load(0, ca, c0, c1);
-        for (int kb0 = 0; kb0 < p.kblocks && ok; kb0 += kScGroup) {
-            float na[kScGroup][4], n0[kScGroup], n1[kScGroup];
-            load(kb0 + kScGroup, na, n0, n1);
-#pragma unroll
-            for (int j = 0; j < kScGroup; ++j) {
-                if (kb0 + j >= p.kblocks) break;
-                if (!tc::mbar_wait(&s.empty[stage], phase ^ 1u, s.abort)) {
-                    ok = false;
-                    break;
-                }
-                uint4* sf = reinterpret_cast<uint4*>(s.sf + (size_t)stage * kSfStageBytes);
-                sf[lane] = make_uint4(ue8m0x4(ca[j][0]), ue8m0x4(ca[j][1]), ue8m0x4(ca[j][2]), ue8m0x4(ca[j][3]));
-                const uint32_t w0 = ue8m0x4(c0[j]), w1 = ue8m0x4(c1[j]);
-                sf[32 + lane] = make_uint4(w0, w0, w0, w0);
-                if (kUp) sf[64 + lane] = make_uint4(w1, w1, w1, w1);
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&s.full[stage]);
-                if (++stage == G::Stages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kScGroup; ++j) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) ca[j][c] = na[j][c];
-                c0[j] = n0[j];
-                c1[j] = n1[j];
-            }
+            for (int i = 0; i < 4; ++i) ca[j][i] = na[j][i];
+            c0[j] = n0[j];
+            c1[j] = n1[j];
         }
     }
     if (!ok) fail(s, p.err);
