@@ -179,12 +179,17 @@ MOE_API moe_status moe_plan_noalloc(const moe_config* cfg, int32_t T, const int3
  * xe[slot_of[t][j]] = x[t] for every placed entry (slot >= 0).  FP8 layers quantise
  * each 1x128 group of the bf16 row with the power-of-two scale 2^s, s the smallest
  * integer with amax <= 448 * 2^s (amax = 0 -> s = 0), e4m3 round-to-nearest-even:
- * xe_scale[row][g] = 2^s.  Rows no entry maps to are not written.
+ * scale(row, g) = 2^s.  Rows no entry maps to are not written.
  * x        device [T][H]: fp32 (MOE_F32) or bf16.
  * xe       device [rows][H]: fp32 / bf16 / e4m3 (out).
- * xe_scale device fp32 [rows][H/128] (out, FP8 only; else NULL). */
+ * xe_scale device fp32 (out, FP8 only; else NULL): with xe_scale_ld == 0 row-major
+ *          [rows][H/128], scale(row, g) = xe_scale[row * H/128 + g]; with xe_scale_ld > 0
+ *          column-major, scale(row, g) = xe_scale[g * xe_scale_ld + row] (xe_scale_ld >=
+ *          rows; the layout moe_layer_dbo keeps internally, where the FFN reads 32
+ *          consecutive rows' scales in one request).  xe_scale_ld < 0: MOE_ERR_INVALID_ARG. */
 MOE_API moe_status moe_dispatch(const moe_config* cfg, int32_t T, const void* x, const int32_t* slot_of,
-                        void* xe, float* xe_scale, int32_t max_ctas, moe_stream_t stream);
+                        void* xe, float* xe_scale, int64_t xe_scale_ld, int32_t max_ctas,
+                        moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_expert_ffn -- every expert's SwiGLU FFN on its rows (the grouped expert GEMMs
@@ -199,15 +204,17 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, int32_t T, const void* x,
  * counts, offsets device int32 [E+S], [E+S+1] (from moe_plan).
  * max_rows  rows of xe / ye (moe_plan_rows); a range beyond it sets MOE_ERR_BAD_INDEX.
  * w13      device [E+S][2I][H]; w2 device [E+S][H][I]; fp32 / bf16 / e4m3.
+ * xe_scale, xe_scale_ld  the activation scales in either layout of moe_dispatch (FP8
+ *          only); a column-major xe_scale_ld below max_rows is MOE_ERR_INVALID_ARG.
  * w13_scale device fp32 [E+S][2I/128][H/128]; w2_scale [E+S][H/128][I/128] (FP8 only).
  * ye       device [max_rows][H] (out).
  * ws       device scratch of moe_ffn_workspace_size(cfg, max_rows) bytes.
  * err_flag device int32 or NULL. */
 MOE_API size_t moe_ffn_workspace_size(const moe_config* cfg, int64_t max_rows);
 MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const int32_t* counts, const int32_t* offsets,
-                          int64_t max_rows, const void* xe, const float* xe_scale, const void* w13,
-                          const float* w13_scale, const void* w2, const float* w2_scale, void* ye,
-                          void* ws, size_t ws_bytes, int32_t* err_flag, int32_t max_ctas,
+                          int64_t max_rows, const void* xe, const float* xe_scale, int64_t xe_scale_ld,
+                          const void* w13, const float* w13_scale, const void* w2, const float* w2_scale,
+                          void* ye, void* ws, size_t ws_bytes, int32_t* err_flag, int32_t max_ctas,
                           moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------

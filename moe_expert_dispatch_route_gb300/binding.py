@@ -76,9 +76,9 @@ _SIGS = {
     "moe_plan_workspace_size": (_SZ, [_CFG, _I32]),
     "moe_plan": (_I32, [_CFG, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _I32, _P]),
     "moe_plan_noalloc": (_I32, [_CFG, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _I32, _P]),
-    "moe_dispatch": (_I32, [_CFG, _I32, _P, _P, _P, _P, _I32, _P]),
+    "moe_dispatch": (_I32, [_CFG, _I32, _P, _P, _P, _P, _I64, _I32, _P]),
     "moe_ffn_workspace_size": (_SZ, [_CFG, _I64]),
-    "moe_expert_ffn": (_I32, [_CFG, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _I32, _P]),
+    "moe_expert_ffn": (_I32, [_CFG, _P, _P, _I64, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P, _I32, _P]),
     "moe_combine": (_I32, [_CFG, _I32, _P, _P, _P, _P, _I32, _P]),
     "moe_dbo_create": (_I32, [ctypes.POINTER(_P)]),
     "moe_dbo_destroy": (None, [_P]),
@@ -168,9 +168,9 @@ def moe_plan_noalloc(cfg, T, topk_ids, capacity, align, counts, offsets, slot_of
                                   _stream(stream)), "moe_plan_noalloc")
 
 
-def moe_dispatch(cfg, T, x, slot_of, xe, xe_scale=None, max_ctas=0, stream=None):
+def moe_dispatch(cfg, T, x, slot_of, xe, xe_scale=None, max_ctas=0, stream=None, xe_scale_ld=0):
     _check(lib().moe_dispatch(ctypes.byref(cfg), T, _ptr(x), _ptr(slot_of), _ptr(xe), _ptr(xe_scale),
-                              max_ctas, _stream(stream)), "moe_dispatch")
+                              xe_scale_ld, max_ctas, _stream(stream)), "moe_dispatch")
 
 
 def moe_ffn_workspace_size(cfg, max_rows) -> int:
@@ -178,11 +178,11 @@ def moe_ffn_workspace_size(cfg, max_rows) -> int:
 
 
 def moe_expert_ffn(cfg, counts, offsets, max_rows, xe, xe_scale, w13, w13_scale, w2, w2_scale, ye, ws,
-                   ws_bytes=0, err_flag=None, max_ctas=0, stream=None):
+                   ws_bytes=0, err_flag=None, max_ctas=0, stream=None, xe_scale_ld=0):
     if ws is not None and not ws_bytes:
         ws_bytes = ws.numel() * ws.element_size()
     _check(lib().moe_expert_ffn(ctypes.byref(cfg), _ptr(counts), _ptr(offsets), max_rows, _ptr(xe),
-                                _ptr(xe_scale), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale),
+                                _ptr(xe_scale), xe_scale_ld, _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale),
                                 _ptr(ye), _ptr(ws), ws_bytes, _ptr(err_flag), max_ctas, _stream(stream)),
            "moe_expert_ffn")
 

@@ -140,14 +140,15 @@ moe_status moe_plan(const moe_config* cfg, int32_t T, const int32_t* topk_ids, i
 }
 
 moe_status moe_dispatch(const moe_config* cfg, int32_t T, const void* x, const int32_t* slot_of,
-                        void* xe, float* xe_scale, int32_t max_ctas, moe_stream_t stream) {
+                        void* xe, float* xe_scale, int64_t xe_scale_ld, int32_t max_ctas,
+                        moe_stream_t stream) {
     moe_status s = check_config(cfg);
     if (s != MOE_OK) return s;
-    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || xe_scale_ld < 0) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     if (!x || !slot_of || !xe || (cfg->dtype == MOE_FP8_E4M3 && !xe_scale)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(xe)) return MOE_ERR_ALIGNMENT;
-    return cuda_status(launch_dispatch(*cfg, T, x, slot_of, xe, xe_scale, grid_cap_of(max_ctas),
+    return cuda_status(launch_dispatch(*cfg, T, x, slot_of, xe, xe_scale, xe_scale_ld, grid_cap_of(max_ctas),
                                        (cudaStream_t)stream));
 }
 
@@ -157,9 +158,9 @@ size_t moe_ffn_workspace_size(const moe_config* cfg, int64_t max_rows) {
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const int32_t* counts, const int32_t* offsets,
-                          int64_t max_rows, const void* xe, const float* xe_scale, const void* w13,
-                          const float* w13_scale, const void* w2, const float* w2_scale, void* ye,
-                          void* ws, size_t ws_bytes, int32_t* err_flag, int32_t max_ctas,
+                          int64_t max_rows, const void* xe, const float* xe_scale, int64_t xe_scale_ld,
+                          const void* w13, const float* w13_scale, const void* w2, const float* w2_scale,
+                          void* ye, void* ws, size_t ws_bytes, int32_t* err_flag, int32_t max_ctas,
                           moe_stream_t stream) {
     moe_status s = check_config(cfg);
     if (s != MOE_OK) return s;
@@ -168,11 +169,13 @@ moe_status moe_expert_ffn(const moe_config* cfg, const int32_t* counts, const in
     if (!counts || !offsets || !xe || !w13 || !w2 || !ye) return MOE_ERR_INVALID_ARG;
     const bool fp8 = cfg->dtype == MOE_FP8_E4M3;
     if (fp8 && (!xe_scale || !w13_scale || !w2_scale)) return MOE_ERR_INVALID_ARG;
+    if (xe_scale_ld < 0 || (xe_scale_ld > 0 && xe_scale_ld < max_rows)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(xe) || !aligned16(w13) || !aligned16(w2) || !aligned16(ye)) return MOE_ERR_ALIGNMENT;
     const size_t need = ffn_scratch_bytes(*cfg, max_rows);
     if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_ALIGNMENT;
-    FfnArgs a{counts, offsets, max_rows, xe, xe_scale, w13, w13_scale, w2, w2_scale, ye, ws, err_flag, 0};
+    FfnArgs a{counts, offsets, max_rows, xe, xe_scale, w13, w13_scale, w2, w2_scale, ye, ws, err_flag, 0,
+              xe_scale_ld};
     return cuda_status(launch_ffn(*cfg, a, grid_cap_of(max_ctas), (cudaStream_t)stream));
 }
 

@@ -284,7 +284,7 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
                 if (plan_dispatch_fusable(c, Tu)) {  // small batch: plan and dispatch in one launch
                     const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
                     ce = launch_plan_dispatch(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, err, xu, xe,
-                                              xe_scale, comm_grid, q);
+                                              xe_scale, L.rows, comm_grid, q);
                 } else {
                     ce = launch_plan(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, nullptr, err,
                                      reinterpret_cast<int32_t*>(b + L.hist), comm_grid, q);
@@ -293,12 +293,12 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
             case MOE_OP_DISPATCH: {
                 if (plan_dispatch_fusable(c, Tu)) break;  // done with the plan
                 const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
-                ce = launch_dispatch(c, Tu, xu, slot_of, xe, xe_scale, comm_grid, q);
+                ce = launch_dispatch(c, Tu, xu, slot_of, xe, xe_scale, L.rows, comm_grid, q);
                 break;
             }
             case MOE_OP_FFN: {
                 FfnArgs fa{counts, offsets, L.rows, xe, xe_scale, a->w13, a->w13_scale, a->w2, a->w2_scale,
-                           ye, b + L.ffn, err, two && u == 1 ? 1 : 0};
+                           ye, b + L.ffn, err, two && u == 1 ? 1 : 0, L.rows};
                 ce = launch_ffn(c, fa, ffn_grid, q);
                 break;
             }
@@ -439,17 +439,18 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
             case MOE_OP_PLAN:
                 if (plan_dispatch_fusable(c, Tu))
                     ce = launch_plan_dispatch(c, Tu, ids, capacity, align, counts, offsets, slot_of, err, act, xe,
-                                              xe_scale, comm_grid, q);
+                                              xe_scale, U.rows, comm_grid, q);
                 else
                     ce = launch_plan(c, Tu, ids, capacity, align, counts, offsets, slot_of, nullptr, err,
                                      reinterpret_cast<int32_t*>(b + U.hist), comm_grid, q);
                 break;
             case MOE_OP_DISPATCH:
-                if (!plan_dispatch_fusable(c, Tu)) ce = launch_dispatch(c, Tu, act, slot_of, xe, xe_scale, comm_grid, q);
+                if (!plan_dispatch_fusable(c, Tu))
+                    ce = launch_dispatch(c, Tu, act, slot_of, xe, xe_scale, U.rows, comm_grid, q);
                 break;
             case MOE_OP_FFN: {
                 FfnArgs fa{counts, offsets, U.rows, xe, xe_scale, a->w13[l], fp8 ? a->w13_scale[l] : nullptr, a->w2[l],
-                           fp8 ? a->w2_scale[l] : nullptr, ye, b + U.ffn, err, two && u == 1 ? 1 : 0};
+                           fp8 ? a->w2_scale[l] : nullptr, ye, b + U.ffn, err, two && u == 1 ? 1 : 0, U.rows};
                 ce = launch_ffn(c, fa, ffn_grid, q);
                 break;
             }

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_copy_kernel(
 // fp8 layers: bf16 row -> e4m3 codes + one power-of-two scale per 1x128 group.
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_fp8_kernel(
     int T, int kk, int H, const uint4* __restrict__ x, const int32_t* __restrict__ slot_of,
-    uint2* __restrict__ xe, float* __restrict__ xe_scale) {
+    uint2* __restrict__ xe, float* __restrict__ xe_scale, int64_t scale_cs) {
     pdl_begin();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -41,12 +41,13 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_fp8_kernel(
         const int t = it / nslices;
         const int vbeg = (it - t * nslices) * 128;
         const int my_slot = lane < kk ? __ldg(slot_of + (size_t)t * kk + lane) : -1;
-        dispatch_fp8_item(kk, nvec, x + (size_t)t * nvec, vbeg, min(nvec, vbeg + 128), my_slot, xe, xe_scale, lane);
+        dispatch_fp8_item(kk, nvec, x + (size_t)t * nvec, vbeg, min(nvec, vbeg + 128), my_slot, xe, xe_scale, scale_cs,
+                          lane);
     }
 }
 
 cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int32_t* slot_of,
-                            void* xe, float* xe_scale, int grid_cap, cudaStream_t st) {
+                            void* xe, float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st) {
     if (T <= 0) return cudaSuccess;
     const int kk = c.top_k + c.num_shared;
     const int nvec_io = c.hidden * io_bytes(c.dtype) / 16;
@@ -55,7 +56,7 @@ cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int
     if (grid > grid_cap) grid = grid_cap;
     if (c.dtype == MOE_FP8_E4M3)
         return launch_pdl(dispatch_fp8_kernel, grid, kDispatchThreads, 0, st, T, kk, c.hidden,
-                          static_cast<const uint4*>(x), slot_of, static_cast<uint2*>(xe), xe_scale);
+                          static_cast<const uint4*>(x), slot_of, static_cast<uint2*>(xe), xe_scale, scale_cs);
     const int nvec = c.hidden * elt_bytes(c.dtype) / 16;
     return launch_pdl(dispatch_copy_kernel, grid, kDispatchThreads, 0, st, T, kk, nvec, static_cast<const uint4*>(x),
                       slot_of, static_cast<uint4*>(xe));

@@ -32,7 +32,7 @@ __device__ __forceinline__ void dispatch_copy_item(int kk, int nvec, const uint4
 // [vbeg, vend) of 8 bf16 each (whole groups), passes of 32 vectors read one ahead.
 __device__ __forceinline__ void dispatch_fp8_item(int kk, int nvec, const uint4* __restrict__ src, int vbeg,
                                                   int vend, int my_slot, uint2* __restrict__ xe,
-                                                  float* __restrict__ xe_scale, int lane) {
+                                                  float* __restrict__ xe_scale, int64_t scale_cs, int lane) {
     const int ngroups = nvec / 16;
     uint4 next = vbeg + lane < vend ? __ldg(src + vbeg + lane) : make_uint4(0u, 0u, 0u, 0u);
     for (int v = vbeg + lane; v - lane < vend; v += 32) {
@@ -68,7 +68,8 @@ __device__ __forceinline__ void dispatch_fp8_item(int kk, int nvec, const uint4*
             const int r = __shfl_sync(0xffffffffu, my_slot, j);
             if (r < 0 || !in) continue;
             xe[(size_t)r * nvec + v] = q;
-            if ((lane & 15) == 0) xe_scale[(size_t)r * ngroups + v / 16] = scale;
+            if ((lane & 15) == 0)
+                xe_scale[scale_cs ? (size_t)(v / 16) * scale_cs + r : (size_t)r * ngroups + v / 16] = scale;
         }
     }
 }

@@ -64,10 +64,13 @@ __device__ __forceinline__ int find_expert(const int* tstart, int NE, int tile) 
 }
 
 template <int DT>
-__device__ __forceinline__ float load_act(const void* p, const float* sc, int64_t row, int kx, int K) {
+// (fp8 scales: row-major [rows][K/128] when sc_cs == 0, else column-major with that stride)
+__device__ __forceinline__ float load_act(const void* p, const float* sc, int64_t row, int kx, int K,
+                                          int64_t sc_cs = 0) {
     if (DT == MOE_F32) return static_cast<const float*>(p)[row * K + kx];
     if (DT == MOE_BF16) return bf16_bits_to_f(static_cast<const uint16_t*>(p)[row * K + kx]);
-    return e4m3_to_f(static_cast<const uint8_t*>(p)[row * K + kx]) * sc[row * (K / kQG) + kx / kQG];
+    return e4m3_to_f(static_cast<const uint8_t*>(p)[row * K + kx]) *
+           sc[sc_cs ? (kx / kQG) * sc_cs + row : row * (K / kQG) + kx / kQG];
 }
 
 // weight element (e, n, kx) of a [NE][N][K] tensor with 128x128 block scales
@@ -83,7 +86,7 @@ __device__ __forceinline__ float load_w(const void* p, const float* sc, int e, i
 template <int DT>
 __global__ void __launch_bounds__(NT) ffn_simt_up_kernel(int NE, int H, int I, const int32_t* counts,
                                                          const int32_t* offsets, int64_t max_rows,
-                                                         const void* xe, const float* xe_scale,
+                                                         const void* xe, const float* xe_scale, int64_t xs_cs,
                                                          const void* w13, const float* w13_scale,
                                                          void* h, float* h_scale, int32_t* err, int reverse) {
     __shared__ int tstart[kMaxExperts + 1];
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(NT) ffn_simt_up_kernel(int NE, int H, int I, c
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int kx = k0 + kq + q;
-                    As[kq + q][r] = (r < rows_here && kx < H) ? load_act<DT>(xe, xe_scale, row0 + r, kx, H) : 0.0f;
+                    As[kq + q][r] = (r < rows_here && kx < H) ? load_act<DT>(xe, xe_scale, row0 + r, kx, H, xs_cs) : 0.0f;
                 }
             }
             {
@@ -268,7 +271,7 @@ cudaError_t launch_simt_dt(const moe_config& c, const FfnArgs& a, int grid, cuda
     if (DT == MOE_FP8_E4M3)
         h_scale = reinterpret_cast<float*>(static_cast<char*>(a.ws) + align_up((size_t)a.max_rows * I, 256));
     ffn_simt_up_kernel<DT><<<grid, NT, 0, st>>>(NE, H, I, a.counts, a.offsets, a.max_rows, a.xe, a.xe_scale,
-                                                a.w13, a.w13_scale, h, h_scale, a.err, a.reverse);
+                                                a.xs_cs, a.w13, a.w13_scale, h, h_scale, a.err, a.reverse);
     ffn_simt_down_kernel<DT><<<grid, NT, 0, st>>>(NE, H, I, a.counts, a.offsets, a.max_rows, h, h_scale, a.w2,
                                                   a.w2_scale, a.ye, a.reverse);
     return cudaGetLastError();

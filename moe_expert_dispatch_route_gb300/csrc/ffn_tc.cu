@@ -66,8 +66,9 @@ constexpr size_t smem_bytes(int stages, int stage_bytes, int sf_bytes) {
 constexpr size_t kSmemBytes = smem_bytes(kStages, kStageBytes, 0);
 template <bool kUp>
 constexpr size_t kF8SmemBytes = smem_bytes(F8<kUp>::Stages, F8<kUp>::StageBytes, kSfStageBytes);
-constexpr int kF8Threads = 352;  // warp 0 TMA, warp 1 MMA, warp 2 scale staging, warps 3..10 epilogue
-constexpr int kF8FirstEpiWarp = 3;
+constexpr int kF8Stagers = 1;    // scale-staging warps (round-robin over the steps; two measured slower)
+constexpr int kF8Threads = 32 * (2 + kF8Stagers + 8);  // TMA, MMA, staging, 8 epilogue warps
+constexpr int kF8FirstEpiWarp = 2 + kF8Stagers;
 constexpr int kScGroup = 8;      // fp8: k-blocks of scales loaded at once
 
 // A tiles are loaded with the smallest box of 16 / 32 / 64 / 128 rows that covers the
@@ -91,9 +92,10 @@ struct TcParams {
     void* out;
     int32_t* err;
     int reverse;
-    const float* a_scale;  // fp8: [max_rows][K/128] row-group scales of A
+    const float* a_scale;  // fp8: row-group scales of A, (row r, group g) at r * a_rs + g * a_cs
+    int64_t a_rs, a_cs;
     const float* b_scale;  // fp8: [NE][NB/128][K/128] block scales of B
-    float* out_scale;      // fp8 up: [max_rows][I/128] scales of the quantised h
+    float* out_scale;      // fp8 up: scales of the quantised h, column-major [I/128][max_rows]
     int dense_rows;        // counts == nullptr: one dense matrix of this many rows
     const void* resid;     // bf16 down: added to the product before rounding ([rows][H])
 };
@@ -523,56 +525,66 @@ __device__ __forceinline__ void cursor_tile(const TcParams& p, const Smem& s, in
     for (int i = 0; i < 4; ++i) {
         const int rr = 32 * i + lane;
         const int64_t row = (int64_t)t.row0 + rr;
-        c.arow[i] = (rr < t.rows && row < p.max_rows) ? p.a_scale + row * ksb : nullptr;
+        c.arow[i] = (rr < t.rows && row < p.max_rows) ? p.a_scale + row * p.a_rs : nullptr;
     }
     const float* bsc = p.b_scale + (size_t)t.e * (p.NB / kF8BK) * ksb;
     c.bs0 = bsc + (size_t)t.nt * ksb;
     c.bs1 = bsc + (size_t)(p.I / kF8BK + t.nt) * ksb;
 }
 
-// Loads the scales of the cursor's step (1.0 past the end) and advances it.
 template <bool kUp>
-__device__ __forceinline__ void cursor_fetch(const TcParams& p, const Smem& s, int total, ScaleCursor& c,
-                                             float (&va)[4], float& v0, float& v1) {
-    const bool in = c.lin < total;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) va[i] = (in && c.arow[i]) ? __ldg(c.arow[i] + c.kb) : 1.0f;
-    v0 = in ? __ldg(c.bs0 + c.kb) : 1.0f;
-    v1 = (in && kUp) ? __ldg(c.bs1 + c.kb) : 1.0f;
-    if (in && ++c.kb == p.kblocks) {
+__device__ __forceinline__ void cursor_next(const TcParams& p, const Smem& s, int total, ScaleCursor& c) {
+    if (c.lin < total && ++c.kb == p.kblocks) {
         c.lin += gridDim.x;
         cursor_tile<kUp>(p, s, total, c);
     }
 }
 
+// Loads the scales of the cursor's step (1.0 past the end), then moves the cursor to
+// this warp's next step (kF8Stagers steps on).
+template <bool kUp>
+__device__ __forceinline__ void cursor_fetch(const TcParams& p, const Smem& s, int total, ScaleCursor& c,
+                                             float (&va)[4], float& v0, float& v1) {
+    const bool in = c.lin < total;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) va[i] = (in && c.arow[i]) ? __ldg(c.arow[i] + c.kb * p.a_cs) : 1.0f;
+    v0 = in ? __ldg(c.bs0 + c.kb) : 1.0f;
+    v1 = (in && kUp) ? __ldg(c.bs1 + c.kb) : 1.0f;
+#pragma unroll
+    for (int k = 0; k < kF8Stagers; ++k) cursor_next<kUp>(p, s, total, c);
+}
+
 // Whole warp: for each stage, its row of the stage's three 32 x 16-byte scale blocks:
 // A (word c of row i = the scale of tile row 32c + i, the layout the MMA reads after
 // the replicating copy), B rows 0-127 and B rows 128-255 (one value each), then the
-// second arrival on full[stage].  The CTA's (tile, k-block) steps form one sequence;
-// scales are loaded kScGroup steps ahead of their use, across tile boundaries, so a
-// load's latency stays hidden even for tiles of a few k-blocks.
+// second arrival on full[stage].  The CTA's (tile, k-block) steps form one sequence,
+// shared out round-robin among the kF8Stagers staging warps (`which` = this warp's
+// turn); each loads its scales kScGroup of its steps ahead of their use, across tile
+// boundaries, so a load's latency stays hidden even for tiles of a few k-blocks.
 template <bool kUp>
-__device__ void scale_stager_f8(const TcParams& p, const Smem& s, int total) {
+__device__ void scale_stager_f8(const TcParams& p, const Smem& s, int total, int which) {
     using G = F8<kUp>;
     const int lane = threadIdx.x & 31;
     const int tiles = blockIdx.x < (unsigned)total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int64_t steps = (int64_t)tiles * p.kblocks;
+    const int steps = tiles * p.kblocks;
     ScaleCursor cur;
     cur.lin = blockIdx.x;
     cursor_tile<kUp>(p, s, total, cur);
+    for (int k = 0; k < which; ++k) cursor_next<kUp>(p, s, total, cur);
     float ca[kScGroup][4], c0[kScGroup], c1[kScGroup];
 #pragma unroll
     for (int j = 0; j < kScGroup; ++j) cursor_fetch<kUp>(p, s, total, cur, ca[j], c0[j], c1[j]);
-    int stage = 0;
-    uint32_t phase = 0;
     bool ok = true;
-    for (int64_t step0 = 0; step0 < steps && ok; step0 += kScGroup) {
+    for (int i0 = 0; i0 * kF8Stagers + which < steps && ok; i0 += kScGroup) {
         float na[kScGroup][4], n0[kScGroup], n1[kScGroup];
 #pragma unroll
         for (int j = 0; j < kScGroup; ++j) cursor_fetch<kUp>(p, s, total, cur, na[j], n0[j], n1[j]);
 #pragma unroll
         for (int j = 0; j < kScGroup; ++j) {
-            if (step0 + j >= steps) break;
+            const int step = (i0 + j) * kF8Stagers + which;
+            if (step >= steps) break;
+            const int stage = step % G::Stages;
+            const uint32_t phase = (uint32_t)(step / G::Stages) & 1u;
             if (!tc::mbar_wait(&s.empty[stage], phase ^ 1u, s.abort)) {
                 ok = false;
                 break;
@@ -585,10 +597,6 @@ __device__ void scale_stager_f8(const TcParams& p, const Smem& s, int total) {
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s.full[stage]);
-            if (++stage == G::Stages) {
-                stage = 0;
-                phase ^= 1u;
-            }
         }
 #pragma unroll
         for (int j = 0; j < kScGroup; ++j) {
@@ -736,7 +744,7 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + row * p.I + t.nt * 128 + 64 * half);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                if (half == 0) p.out_scale[row * (p.I / kF8BK) + t.nt] = scalbnf(1.0f, se);
+                if (half == 0) p.out_scale[(int64_t)t.nt * p.max_rows + row] = scalbnf(1.0f, se);
             }
         } else {
             uint32_t a0[32], a1[32];  // columns 64*half .. +63 of the 128-wide tile
@@ -810,8 +818,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_
         if (lane == 0) producer_f8<kUp>(p, s, total);
     } else if (warp == 1) {
         if (lane == 0) mma_issuer_f8<kUp>(p, s, total, tmem_base);
-    } else if (warp == 2) {
-        scale_stager_f8<kUp>(p, s, total);
+    } else if (warp < kF8FirstEpiWarp) {
+        scale_stager_f8<kUp>(p, s, total, warp - 2);
     } else {
         epilogue_f8<kUp>(p, s, total, tmem_base);
     }
@@ -920,6 +928,8 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     up.err = a.err;
     up.reverse = a.reverse;
     up.a_scale = a.xe_scale;
+    up.a_rs = a.xs_cs ? 1 : H / kF8BK;  // see FfnArgs::xs_cs
+    up.a_cs = a.xs_cs ? a.xs_cs : 1;
     up.b_scale = a.w13_scale;
     up.out_scale = h_scale;
     TcParams dn = up;
@@ -932,7 +942,9 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     dn.NB = H;
     dn.ntn = H / (fp8 ? F8<false>::N : kBN);
     dn.out = a.ye;
-    dn.a_scale = h_scale;
+    dn.a_scale = h_scale;  // written column-major by the up kernel
+    dn.a_rs = 1;
+    dn.a_cs = a.max_rows;
     dn.b_scale = a.w2_scale;
     dn.out_scale = nullptr;
     cudaError_t e = fp8 ? launch_one<true, true>(up, grid, st) : launch_one<true, false>(up, grid, st);

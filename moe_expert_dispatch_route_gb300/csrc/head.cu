@@ -18,7 +18,7 @@ template <bool kFp8>
 __global__ void __launch_bounds__(kPlanThreads) plan_dispatch_kernel(
     int T, int k, int S, int E, int capacity, int align, const int32_t* __restrict__ ids,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot_of, int32_t* err,
-    const uint4* __restrict__ x, void* __restrict__ xe, float* __restrict__ xe_scale, int nvec) {
+    const uint4* __restrict__ x, void* __restrict__ xe, float* __restrict__ xe_scale, int64_t scale_cs, int nvec) {
     extern __shared__ int head_sm[];
     pdl_begin();
     const int kk = k + S;
@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_dispatch_kernel(
         const int my_slot = lane < kk ? slot_sm[t * kk + lane] : -1;
         if (kFp8)
             dispatch_fp8_item(kk, nvec, x + (size_t)t * nvec, vbeg, min(nvec, vbeg + 128), my_slot,
-                              static_cast<uint2*>(xe), xe_scale, lane);
+                              static_cast<uint2*>(xe), xe_scale, scale_cs, lane);
         else
             dispatch_copy_item(kk, nvec, x + (size_t)t * nvec, vbeg, my_slot, static_cast<uint4*>(xe), lane);
     }
@@ -49,7 +49,7 @@ bool plan_dispatch_fusable(const moe_config& c, int T) { return T > 0 && plan_nu
 template <bool kFp8>
 static cudaError_t launch_fused(const moe_config& c, int T, const int32_t* ids, int capacity, int align,
                                 int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* err, const void* x,
-                                void* xe, float* xe_scale, int grid_cap, cudaStream_t st) {
+                                void* xe, float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st) {
     static int configured_dev = -1;
     const int kk = c.top_k + c.num_shared;
     const size_t smem = 2 * (size_t)T * kk * sizeof(int);
@@ -68,17 +68,17 @@ static cudaError_t launch_fused(const moe_config& c, int T, const int32_t* ids, 
     if (grid < 1) grid = 1;
     return launch_pdl(plan_dispatch_kernel<kFp8>, grid, kPlanThreads, smem, st, T, c.top_k, c.num_shared,
                       c.num_experts, capacity, align, ids, counts, offsets, slot_of, err,
-                      static_cast<const uint4*>(x), xe, xe_scale, nvec);
+                      static_cast<const uint4*>(x), xe, xe_scale, scale_cs, nvec);
 }
 
 cudaError_t launch_plan_dispatch(const moe_config& c, int T, const int32_t* ids, int capacity, int align,
                                  int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* err, const void* x,
-                                 void* xe, float* xe_scale, int grid_cap, cudaStream_t st) {
+                                 void* xe, float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st) {
     if (c.dtype == MOE_FP8_E4M3)
         return launch_fused<true>(c, T, ids, capacity, align, counts, offsets, slot_of, err, x, xe, xe_scale,
-                                  grid_cap, st);
-    return launch_fused<false>(c, T, ids, capacity, align, counts, offsets, slot_of, err, x, xe, xe_scale, grid_cap,
-                               st);
+                                  scale_cs, grid_cap, st);
+    return launch_fused<false>(c, T, ids, capacity, align, counts, offsets, slot_of, err, x, xe, xe_scale, scale_cs,
+                               grid_cap, st);
 }
 
 }  // namespace moe

@@ -34,11 +34,14 @@ cudaError_t launch_plan(const moe_config& c, int T, const int32_t* ids, int capa
 bool plan_dispatch_fusable(const moe_config& c, int T);
 cudaError_t launch_plan_dispatch(const moe_config& c, int T, const int32_t* ids, int capacity, int align,
                                  int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* err, const void* x,
-                                 void* xe, float* xe_scale, int grid_cap, cudaStream_t st);
+                                 void* xe, float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st);
 
-// dispatch.cu / combine.cu
+// dispatch.cu / combine.cu.  fp8 row scales: scale (row r, group g) sits at
+// xe_scale[r * (H/128) + g] when scale_cs == 0 (the ABI's row-major layout), else at
+// xe_scale[g * scale_cs + r] (column-major, as the layer keeps them internally: the FFN
+// then reads 32 consecutive rows' scales in one request).
 cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int32_t* slot_of,
-                            void* xe, float* xe_scale, int grid_cap, cudaStream_t st);
+                            void* xe, float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st);
 cudaError_t launch_combine(const moe_config& c, int T, const void* ye, const float* w,
                            const int32_t* slot_of, void* y, int grid_cap, cudaStream_t st,
                            const void* resid = nullptr);
@@ -58,7 +61,8 @@ struct FfnArgs {
     void* ye;
     void* ws;
     int32_t* err;
-    int reverse;  // walk experts in descending order (L2 reuse across ubatches)
+    int reverse;     // walk experts in descending order (L2 reuse across ubatches)
+    int64_t xs_cs;   // layout of xe_scale: 0 = row-major, else column-major with this column stride
 };
 cudaError_t launch_ffn(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
 

@@ -49,13 +49,14 @@ def test_invalid_arguments_rejected_on_host():
     assert L.moe_route(ctypes.byref(bad), 4, 16, None, 16, 16, 0, None) == 1
     assert L.moe_route(ctypes.byref(cfg), 4, None, None, 16, 16, 0, None) == 1
     assert L.moe_route(ctypes.byref(cfg), 0, None, None, None, None, 0, None) == 0  # empty batch
-    assert L.moe_dispatch(ctypes.byref(cfg), 4, 8, 16, 16, None, 0, None) == 3        # misaligned x
+    assert L.moe_dispatch(ctypes.byref(cfg), 4, 8, 16, 16, None, 0, 0, None) == 3     # misaligned x
+    assert L.moe_dispatch(ctypes.byref(cfg), 4, 16, 16, 16, None, -1, 0, None) == 1   # negative scale ld
     g = B.config_of(W.DSV3)
     g.n_group = 7  # 256 % 7 != 0
     assert L.moe_route(ctypes.byref(g), 4, 16, None, 16, 16, 0, None) == 1
     f = B.config_of(W.QWEN3_PREFILL)
     f.hidden = 2000  # fp8 needs multiples of 128
-    assert L.moe_dispatch(ctypes.byref(f), 4, 16, 16, 16, 16, 0, None) == 3
+    assert L.moe_dispatch(ctypes.byref(f), 4, 16, 16, 16, 16, 0, 0, None) == 3
     # plan: workspace required when the batch spans several chunks
     assert B.moe_plan_workspace_size(cfg, 100000) > 0
     assert L.moe_plan(ctypes.byref(cfg), 100000, 16, 0, 128, 16, 16, 16, 16, 16, None, 0, 0, None) == 4

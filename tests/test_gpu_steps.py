@@ -148,6 +148,14 @@ def test_dispatch_matches_oracle_bit_exact(wl):
         torch.cuda.synchronize()
         assert np.array_equal(xe.cpu().numpy()[used], ref["xe_q"][used])
         assert np.array_equal(xs.cpu().numpy()[used], ref["xe_s"][used])
+        # column-major scales (the layer's internal layout), with a stride above rows
+        ld = rows + 7
+        xsc = torch.zeros(H // 128, ld, dtype=torch.float32, device=DEV)
+        xe.zero_()
+        B.moe_dispatch(cfg, wl.T, x.to(DEV), torch.as_tensor(p["slot_of"], device=DEV), xe, xsc, xe_scale_ld=ld)
+        torch.cuda.synchronize()
+        assert np.array_equal(xe.cpu().numpy()[used], ref["xe_q"][used])
+        assert np.array_equal(xsc.cpu().numpy()[:, :rows].T[used], ref["xe_s"][used])
     else:
         tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
         xe = torch.zeros(rows, H, dtype=tdt, device=DEV)
@@ -170,13 +178,17 @@ def _ffn_inputs(wl, align=128, capacity=0):
     return x, W_, ids, w, p, d
 
 
-def _run_ffn_gpu(wl, W_, p, d, max_ctas=0):
+def _run_ffn_gpu(wl, W_, p, d, max_ctas=0, scale_ld=0):
     cfg = B.config_of(wl)
     rows = p["rows"]
     H = wl.hidden
     if wl.dtype == "fp8":
         xe = torch.as_tensor(d["xe_q"], device=DEV)
         xs = torch.as_tensor(d["xe_s"], device=DEV)
+        if scale_ld:  # column-major: scale(row, g) at g * scale_ld + row
+            xsc = torch.zeros(H // 128, scale_ld, dtype=torch.float32, device=DEV)
+            xsc[:, :rows] = xs.t()
+            xs = xsc
         w13, w13s, w2, w2s = (W_[k].to(DEV) for k in ("w13_q", "w13_s", "w2_q", "w2_s"))
         ye = torch.zeros(rows, H, dtype=torch.bfloat16, device=DEV)
     else:
@@ -190,10 +202,20 @@ def _run_ffn_gpu(wl, W_, p, d, max_ctas=0):
     ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     B.moe_expert_ffn(cfg, torch.as_tensor(p["counts"], device=DEV), torch.as_tensor(p["offsets"], device=DEV),
-                     rows, xe, xs, w13, w13s, w2, w2s, ye, ws, wsb, err, max_ctas)
+                     rows, xe, xs, w13, w13s, w2, w2s, ye, ws, wsb, err, max_ctas, xe_scale_ld=scale_ld)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     return np_f32(ye)
+
+
+@pytest.mark.parametrize("wl", [w for w in FFN_CASES if w.dtype == "fp8"], ids=lambda w: w.name)
+def test_expert_ffn_scale_layouts_agree(wl):
+    """Row-major and column-major activation scales give the same ye, bit for bit."""
+    x, W_, ids, w, p, d = _ffn_inputs(wl)
+    a = _run_ffn_gpu(wl, W_, p, d)
+    b = _run_ffn_gpu(wl, W_, p, d, scale_ld=p["rows"] + 5)
+    used = p["token_of"] >= 0
+    assert np.array_equal(a[used], b[used])
 
 
 @pytest.mark.parametrize("wl", FFN_CASES, ids=lambda w: w.name)
