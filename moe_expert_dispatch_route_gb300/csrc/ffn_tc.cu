@@ -81,7 +81,8 @@ __host__ __device__ constexpr int a_box_rows(int i) { return 16 << i; }
 
 struct TcParams {
     CUtensorMap tmA[kNumABoxes];  // activations [max_rows][K], box heights 16, 32, 64, 128
-    CUtensorMap tmB;              // weights [NE * NB][K]
+    CUtensorMap tmB;  // up: W13 viewed as [2 NE halves][I][K], box = one n-block of gate and of up rows;
+                      // down: W2 [NE * H][K], box = the tile's N rows
     const int32_t* counts;
     const int32_t* offsets;
     int NE, K, kblocks;
@@ -216,14 +217,7 @@ __device__ void producer(const TcParams& p, const Smem& s, int total) {
     bool ok = true;
     for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
         const Tile t = decode_tile(p, s, total, lin);
-        int b0, b1;
-        if (kUp) {
-            b0 = t.e * p.NB + t.nt * 128;
-            b1 = t.e * p.NB + p.I + t.nt * 128;
-        } else {
-            b0 = t.e * p.NB + t.nt * kBN;
-            b1 = b0 + 128;
-        }
+        const int b0 = t.e * p.NB + t.nt * kBN;  // down: first weight row of the tile
         int abox = 0;
         while (abox < kNumABoxes - 1 && a_box_rows(abox) < t.rows) ++abox;
         const int abox_rows = a_box_rows(abox);
@@ -236,8 +230,10 @@ __device__ void producer(const TcParams& p, const Smem& s, int total) {
             uint8_t* b = a + kABytes;
             tc::mbar_arrive_expect_tx(&s.full[stage], (uint32_t)(abox_rows * 128 + kBBytes));
             tc::tma_load_2d(a, &p.tmA[abox], &s.full[stage], kb * kKElems, t.row0);
-            tc::tma_load_2d(b, &p.tmB, &s.full[stage], kb * kKElems, b0);
-            tc::tma_load_2d(b + kBBytes / 2, &p.tmB, &s.full[stage], kb * kKElems, b1);
+            if (kUp)  // gate rows n0..n0+127 then up rows I+n0.. in one box
+                tc::tma_load_3d(b, &p.tmB, &s.full[stage], kb * kKElems, t.nt * 128, 2 * t.e);
+            else
+                tc::tma_load_2d(b, &p.tmB, &s.full[stage], kb * kKElems, b0);
             pending |= 1u << stage;
             pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {
@@ -468,8 +464,7 @@ __device__ void producer_f8(const TcParams& p, const Smem& s, int total) {
     bool ok = true;
     for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
         const Tile t = decode_tile(p, s, total, lin);
-        const int b0 = t.e * p.NB + t.nt * 128;
-        const int b1 = t.e * p.NB + p.I + t.nt * 128;  // up kernel: the up rows
+        const int b0 = t.e * p.NB + t.nt * 128;  // down: first weight row of the tile
         int abox = 0;
         while (abox < kNumABoxes - 1 && a_box_rows(abox) < t.rows) ++abox;
         const uint32_t tx = (uint32_t)(a_box_rows(abox) * kF8BK + G::N * kF8BK);
@@ -482,8 +477,10 @@ __device__ void producer_f8(const TcParams& p, const Smem& s, int total) {
             uint8_t* b = a + kBM * kF8BK;
             tc::mbar_arrive_expect_tx(&s.full[stage], tx);
             tc::tma_load_2d(a, &p.tmA[abox], &s.full[stage], kb * kF8BK, t.row0);
-            tc::tma_load_2d(b, &p.tmB, &s.full[stage], kb * kF8BK, b0);
-            if (kUp) tc::tma_load_2d(b + 128 * kF8BK, &p.tmB, &s.full[stage], kb * kF8BK, b1);
+            if (kUp)  // gate rows n0..n0+127 then up rows I+n0.. in one box
+                tc::tma_load_3d(b, &p.tmB, &s.full[stage], kb * kF8BK, t.nt * 128, 2 * t.e);
+            else
+                tc::tma_load_2d(b, &p.tmB, &s.full[stage], kb * kF8BK, b0);
             pending |= 1u << stage;
             pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
             if (++stage == G::Stages) {
@@ -860,6 +857,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, b
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// W13 [NE][2I][K] as a 3-D tensor [2 NE][I][K] (gate half 2e, up half 2e + 1) with a
+// box of one 128-byte row x 128 rows x both halves: one copy brings the up tile's B.
+bool make_map_w13(CUtensorMap* m, const void* base, uint64_t K, uint64_t I, uint64_t NE, bool fp8) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const uint64_t elt = fp8 ? 1 : 2;
+    cuuint64_t dims[3] = {K, I, 2 * NE};
+    cuuint64_t strides[2] = {K * elt, I * K * elt};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elt), 128, 2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool kUp, bool kFp8>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
     static int configured_dev = -1;
@@ -913,7 +925,7 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     for (int i = 0; i < kNumABoxes; ++i)
         if (!make_map(&up.tmA[i], a.xe, (uint64_t)H, (uint64_t)a.max_rows, fp8, a_box_rows(i)))
             return cudaErrorInvalidValue;
-    if (!make_map(&up.tmB, a.w13, (uint64_t)H, (uint64_t)NE * 2 * I, fp8)) return cudaErrorInvalidValue;
+    if (!make_map_w13(&up.tmB, a.w13, (uint64_t)H, (uint64_t)I, (uint64_t)NE, fp8)) return cudaErrorInvalidValue;
     up.counts = a.counts;
     up.offsets = a.offsets;
     up.NE = NE;
@@ -936,7 +948,8 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     for (int i = 0; i < kNumABoxes; ++i)
         if (!make_map(&dn.tmA[i], h, (uint64_t)I, (uint64_t)a.max_rows, fp8, a_box_rows(i)))
             return cudaErrorInvalidValue;
-    if (!make_map(&dn.tmB, a.w2, (uint64_t)I, (uint64_t)NE * H, fp8)) return cudaErrorInvalidValue;
+    if (!make_map(&dn.tmB, a.w2, (uint64_t)I, (uint64_t)NE * H, fp8, fp8 ? F8<false>::N : kBN))
+        return cudaErrorInvalidValue;
     dn.K = I;
     dn.kblocks = I / kelems;
     dn.NB = H;
@@ -970,7 +983,7 @@ cudaError_t launch_standin(const moe_config& c, int rows, const void* x, const v
     TcParams p{};
     for (int i = 0; i < kNumABoxes; ++i)
         if (!make_map(&p.tmA[i], x, (uint64_t)H, (uint64_t)rows, false, a_box_rows(i))) return cudaErrorInvalidValue;
-    if (!make_map(&p.tmB, wa, (uint64_t)H, (uint64_t)H, false)) return cudaErrorInvalidValue;
+    if (!make_map(&p.tmB, wa, (uint64_t)H, (uint64_t)H, false, kBN)) return cudaErrorInvalidValue;
     p.counts = nullptr;
     p.offsets = nullptr;
     p.dense_rows = rows;
