@@ -425,9 +425,12 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
                                  : ws + S.pp[(l - 1) % 2] + t0[u] * rowb;
         char* xout = l == L - 1 ? static_cast<char*>(a->out) + t0[u] * rowb : ws + S.pp[l % 2] + t0[u] * rowb;
         const int Tu = tn[u];
-        const bool overlapped = two;
-        const int comm_grid = overlapped ? comm_cap : sms * 8;
-        const int ffn_grid = overlapped ? ffn_cap : sms * 8;
+        // the SM budget applies where a comm step runs beside an FFN: ubatch 1's route,
+        // plan and dispatch (beside F0) and ubatch 0's combine (beside F1).  Ubatch 0's
+        // head and ubatch 1's combine run beside a stand-in block only and take the GPU.
+        const bool beside_ffn = two && (op.op == MOE_OP_COMBINE ? u == 0 : u == 1);
+        const int comm_grid = beside_ffn ? comm_cap : sms * 8;
+        const int ffn_grid = two ? ffn_cap : sms * 8;
         cudaError_t ce = cudaSuccess;
         switch (op.op) {
             case MOE_OP_RECORD: ce = cudaEventRecord(h->ev[op.ev], q); break;
