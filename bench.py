@@ -522,35 +522,65 @@ def ffn_roofline(B, wl, cfg, inp, dev, args, comm_sms, compute):
 
 
 def run_e2e(B, wl, cfg, inp, args_c, handle, comm, compute, enqueue, logits, x, y, args, world):
-    """Same metric with host buffers: every step copies logits and x from pinned host
-    memory, runs the layer through the C ABI and copies y back."""
+    """Same metric with host buffers, as a serving loop runs it: every step copies its
+    logits and x from pinned host memory, runs the layer through the C ABI and copies y
+    back.  Uploads and downloads run on streams of their own with two device buffer
+    sets, so step i+1's inputs go up while layer i computes and step i's y comes down
+    while layer i+1 computes; the timed region holds every step's copies."""
     h_logits = logits.cpu().pin_memory()
     h_x = x.cpu().pin_memory()
-    h_y = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    h_y = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(2)]
+    Wd = {k: v for k, v in inp.items() if k.startswith("w")}
+    lg2, x2, y2 = torch.empty_like(logits), torch.empty_like(x), torch.empty_like(y)
+    ws2 = torch.empty(0, dtype=torch.uint8, device=logits.device)
+    # the second buffer set shares the workspace: layers run one after another
+    a2 = B.layer_args(lg2, x2, Wd, y2, None, None, ws2)
+    for f in ("topk_ids", "topk_w", "err_flag", "workspace", "workspace_bytes"):
+        setattr(a2, f, getattr(args_c, f))
+    sets = [(logits, x, y, args_c), (lg2, x2, y2, a2)]
+    up = torch.cuda.Stream(device=logits.device)
+    down = torch.cuda.Stream(device=logits.device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_out:
+        e.record(down)
 
-    def step():
-        with torch.cuda.stream(compute):
-            logits.copy_(h_logits, non_blocking=True)
-            x.copy_(h_x, non_blocking=True)
-            enqueue(cs=compute)
-            h_y.copy_(y, non_blocking=True)
+    def step(i):
+        b = i % 2
+        lg_b, x_b, y_b, a_b = sets[b]
+        up.wait_event(ev_out[b])  # y of step i-2 is down: buffer set b is free
+        with torch.cuda.stream(up):
+            lg_b.copy_(h_logits, non_blocking=True)
+            x_b.copy_(h_x, non_blocking=True)
+        ev_in[b].record(up)
+        compute.wait_event(ev_in[b])
+        enqueue(a=a_b, cs=compute)
+        ev_done[b].record(compute)
+        down.wait_event(ev_done[b])
+        with torch.cuda.stream(down):
+            h_y[b].copy_(y_b, non_blocking=True)
+        ev_out[b].record(down)
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(compute)
-    for _ in range(args.steps):
-        step()
+    up.wait_event(e0)
+    for i in range(args.steps):
+        step(i)
+    compute.wait_event(ev_out[(args.steps - 1) % 2])  # the last y is on the host
     e1.record(compute)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     bi = h_logits.numel() * h_logits.element_size() + h_x.numel() * h_x.element_size()
-    bo = h_y.numel() * h_y.element_size()
+    bo = h_y[0].numel() * h_y[0].element_size()
     return {"value": round(wl.T * world / (ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 5)}
+            "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 5),
+            "pipeline": "uploads and downloads on streams of their own, two buffer sets"}
 
 
 # --------------------------------------------------------------------------- oracle legs
