@@ -1,13 +1,15 @@
 // Grouped expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// Two persistent, warp-specialised kernels, one CTA per SM:
+// Two persistent, warp-specialised kernels per layer type, one CTA per SM (the bf16
+// kernels are described here, the block-scaled FP8 ones with their code below):
 //   up   : acc[128 x 256] = xe[rows] . [W13 gate rows n0..n0+127 | up rows I+n0..]^T,
 //          epilogue h = silu(g) * u -> bf16 h[rows][n0..n0+127]
 //   down : acc[128 x 256] = h[rows] . W2[e][n0..n0+255]^T, epilogue -> bf16 ye
 // A tile = 128 rows of one expert's segment (rows past the segment are computed and
-// discarded), B tile = 256 weight rows; k-blocks of 64 bf16 (one 128-byte swizzle
-// row).  Tiles (expert, n-block, m-block) are derived on the device from counts and
-// offsets, so no host synchronisation is needed and the launch is graph-capturable.
+// discarded), B tile = 256 weight rows, one TMA box (W13 is addressed as a 3-D tensor
+// so that the gate and up n-blocks come in one box); k-blocks of 64 bf16 (one 128-byte
+// swizzle row).  Tiles (expert, n-block, m-block) are derived on the device from counts
+// and offsets, so no host synchronisation is needed and the launch is graph-capturable.
 //
 // Roles (192 threads):
 //   warp 0 (one lane)  TMA producer: 4-stage ring of {A 16 KB, B 32 KB}
