@@ -57,6 +57,11 @@ def test_invalid_arguments_rejected_on_host():
     f = B.config_of(W.QWEN3_PREFILL)
     f.hidden = 2000  # fp8 needs multiples of 128
     assert L.moe_dispatch(ctypes.byref(f), 4, 16, 16, 16, 16, 0, 0, None) == 3
+    # expert FFN: a column-major scale stride must cover max_rows (and not be negative)
+    ffn = lambda ld: L.moe_expert_ffn(ctypes.byref(f8), 16, 16, 100, 16, 16, ld, 16, 16, 16, 16, 16, 16, 1 << 30,
+                                      None, 0, None)
+    f8 = B.config_of(W.QWEN3_PREFILL)
+    assert ffn(5) == 1 and ffn(-1) == 1
     # plan: workspace required when the batch spans several chunks
     assert B.moe_plan_workspace_size(cfg, 100000) > 0
     assert L.moe_plan(ctypes.byref(cfg), 100000, 16, 0, 128, 16, 16, 16, 16, 16, None, 0, 0, None) == 4
