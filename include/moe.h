@@ -161,7 +161,8 @@ MOE_API moe_status moe_plan(const moe_config* cfg, int32_t T, const int32_t* top
  * scratch (per-chunk expert histograms) is a fixed 256 KiB array inside the
  * library's device memory, held by every GPU that loads the library until the
  * process exits.  Limit: moe_plan_workspace_size(cfg, T) <= 262144 bytes, i.e.
- * ceil(T / floor(4096 / (k+S))) * (E+S) <= 65536; a larger T returns
+ * ceil(T / floor(1024 / (k+S))) * (E+S) <= 65536 (a batch of more than 4096
+ * entries is cut into chunks of about 1024; a smaller one needs no scratch); a larger T returns
  * MOE_ERR_WORKSPACE before anything is enqueued (MOE_DEBUG=1 prints why).
  * The first call on a device that needs the scratch looks up the array's device
  * address with that device current; make that first call before any stream capture.

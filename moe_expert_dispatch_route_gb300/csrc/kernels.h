@@ -24,7 +24,7 @@ cudaError_t launch_route(const moe_config& c, int T, const float* logits, const 
                          int32_t* ids, float* w, int grid_cap, cudaStream_t st);
 
 // plan.cu
-int plan_tokens_per_chunk(const moe_config& c);
+int plan_tokens_per_chunk(const moe_config& c, int T);
 int plan_num_chunks(const moe_config& c, int T);
 cudaError_t launch_plan(const moe_config& c, int T, const int32_t* ids, int capacity, int align,
                         int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* token_of,

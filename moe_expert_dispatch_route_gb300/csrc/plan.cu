@@ -1,7 +1,8 @@
 // moe_plan kernels: a deterministic, stable counting sort of the (token, choice)
 // entries by expert; slot assignment uses only order-independent integer adds.
 //
-// The entries are cut into chunks of whole tokens (about 4096 entries each).
+// A batch of up to 4096 entries is one chunk; a larger one is cut into chunks of whole
+// tokens of about 1024 entries each, so that the passes spread over many SMs.
 //   pass 1 (plan_count_kernel, skipped when there is one chunk): one CTA per chunk
 //           writes the chunk's per-expert histogram to the workspace.
 //   pass 2 (plan_assign_kernel): one CTA per chunk re-derives the global counts and
@@ -18,14 +19,14 @@
 
 namespace moe {
 
-int plan_tokens_per_chunk(const moe_config& c) {
-    int kk = c.top_k + c.num_shared;
-    int tpc = kPlanEntriesPerChunk / kk;
+int plan_tokens_per_chunk(const moe_config& c, int T) {
+    const int kk = c.top_k + c.num_shared;
+    const int tpc = ((int64_t)T * kk <= kPlanEntriesPerChunk ? kPlanEntriesPerChunk : kPlanEntriesPerChunkMulti) / kk;
     return tpc < 1 ? 1 : tpc;
 }
 
 int plan_num_chunks(const moe_config& c, int T) {
-    int tpc = plan_tokens_per_chunk(c);
+    const int tpc = plan_tokens_per_chunk(c, T);
     return (T + tpc - 1) / tpc;
 }
 
@@ -64,7 +65,7 @@ cudaError_t launch_plan(const moe_config& c, int T, const int32_t* ids, int capa
                         int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* token_of,
                         int32_t* err, int32_t* hist_ws, int grid_cap, cudaStream_t st) {
     (void)grid_cap;  // one CTA per chunk: the plan is latency-bound and needs few CTAs
-    const int tpc = plan_tokens_per_chunk(c);
+    const int tpc = plan_tokens_per_chunk(c, T);
     int nchunks = (T + tpc - 1) / tpc;
     if (nchunks < 1) nchunks = 1;  // T == 0 still writes counts and offsets
     if (nchunks > 1) {

@@ -8,7 +8,8 @@ namespace moe {
 
 constexpr int kPlanThreads = 256;
 constexpr int kPlanWarps = kPlanThreads / 32;
-constexpr int kPlanEntriesPerChunk = 4096;
+constexpr int kPlanEntriesPerChunk = 4096;       // a batch up to this many entries is one chunk
+constexpr int kPlanEntriesPerChunkMulti = 1024;  // larger batches: chunks of about this many
 
 // Expert of entry (t, j); -1 for a routed id outside [0, E).
 __device__ __forceinline__ int entry_expert(const int32_t* ids, int t, int j, int k, int E) {
