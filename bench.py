@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -180,15 +181,23 @@ def launches_per_step(wl, split_two: bool) -> int:
     return n
 
 
+def code_only(text: str) -> str:
+    """C/C++ source without comments, whitespace runs collapsed (the sources hold no
+    comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def ffn_source_hash() -> str:
-    """Hash of the device sources of the FFN kernels (a profile's DRAM counters apply
-    only while these are unchanged)."""
+    """Hash of the code (comments aside) of the FFN kernels' device sources: a
+    profile's DRAM counters apply only while it is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_dispatch_route_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.startswith("ffn") or name in ("common.cuh", "tc_ptx.cuh"):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name)) as f:
+                h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
