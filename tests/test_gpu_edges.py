@@ -53,6 +53,13 @@ ODD = [
     W.Workload("odd_fp8", T=19, hidden=384, inter=256, num_experts=40, num_shared=1, top_k=4, dtype="fp8", seed=34),
     W.Workload("grouped_one", T=23, hidden=512, inter=256, num_experts=64, num_shared=0, top_k=6,
                gate="sigmoid_grouped", n_group=4, topk_group=1, dtype="bf16", seed=35),
+    # the tensor-core kernels with one or two k-blocks per tile and several tiles per CTA
+    # (160 experts: the FP8 down kernel has ~640 tiles of a single k-block), so the FP8
+    # scale staging looks ahead across many tile boundaries
+    W.Workload("short_k_fp8", T=400, hidden=512, inter=128, num_experts=160, num_shared=1, top_k=4, dtype="fp8",
+               seed=36),
+    W.Workload("short_k_bf16", T=400, hidden=512, inter=128, num_experts=160, num_shared=1, top_k=4, dtype="bf16",
+               seed=37),
 ]
 
 
