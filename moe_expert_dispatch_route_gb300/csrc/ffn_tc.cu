@@ -44,16 +44,17 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kF8BK = 128;  // e4m3 elements per k-block = one 128-wide scale block
 
-// FP8 tile geometry.  up: 128 x 256 tiles (gate 128 | up 128 columns, so that a whole
-// 1x128 group of h is formed in one tile), one accumulator, 4 stages of 48 KB.  down:
-// 128 x 128 tiles, two accumulators (the epilogue of one tile overlaps the next tile's
-// MMAs), 6 stages of 32 KB.  Scale factors of each stage are staged in shared memory
-// (kSfStageBytes) and copied into TMEM slot kSfCol + 16 * stage.
+// FP8 tile geometry: 128 x 256 tiles (up: gate 128 | up 128 columns, so that a whole
+// 1x128 group of h is formed in one tile; down: two 128-row n-blocks of W2), one
+// accumulator (the scale slots take the rest of TMEM), 4 stages of 48 KB.  Scale factors
+// of each stage are staged in shared memory (kSfStageBytes) and copied into TMEM slot
+// kSfCol + 16 * stage.  (128 x 128 down tiles with two accumulators and 6 stages of
+// 32 KB measured slower.)
 template <bool kUp>
 struct F8 {
-    static constexpr int N = kUp ? 256 : 128;
-    static constexpr int AccBufs = kUp ? 1 : 2;
-    static constexpr int Stages = kUp ? 4 : 6;
+    static constexpr int N = 256;
+    static constexpr int AccBufs = 1;
+    static constexpr int Stages = 4;
     static constexpr int StageBytes = kBM * kF8BK + N * kF8BK;
 };
 constexpr int kSfCol = 256;
@@ -466,7 +467,7 @@ __device__ void producer_f8(const TcParams& p, const Smem& s, int total) {
     bool ok = true;
     for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
         const Tile t = decode_tile(p, s, total, lin);
-        const int b0 = t.e * p.NB + t.nt * 128;  // down: first weight row of the tile
+        const int b0 = t.e * p.NB + t.nt * G::N;  // down: first weight row of the tile
         int abox = 0;
         while (abox < kNumABoxes - 1 && a_box_rows(abox) < t.rows) ++abox;
         const uint32_t tx = (uint32_t)(a_box_rows(abox) * kF8BK + G::N * kF8BK);
@@ -526,9 +527,13 @@ __device__ __forceinline__ void cursor_tile(const TcParams& p, const Smem& s, in
         const int64_t row = (int64_t)t.row0 + rr;
         c.arow[i] = (rr < t.rows && row < p.max_rows) ? p.a_scale + row * p.a_rs : nullptr;
     }
+    // B rows 0-127 and 128-255 of the tile: up, the gate and the up n-block; down, two
+    // consecutive 128-row blocks of W2
     const float* bsc = p.b_scale + (size_t)t.e * (p.NB / kF8BK) * ksb;
-    c.bs0 = bsc + (size_t)t.nt * ksb;
-    c.bs1 = bsc + (size_t)(p.I / kF8BK + t.nt) * ksb;
+    const int nb0 = kUp ? t.nt : t.nt * (F8<kUp>::N / 128);
+    const int nb1 = kUp ? p.I / kF8BK + t.nt : nb0 + 1;
+    c.bs0 = bsc + (size_t)nb0 * ksb;
+    c.bs1 = bsc + (size_t)nb1 * ksb;
 }
 
 template <bool kUp>
@@ -548,7 +553,7 @@ __device__ __forceinline__ void cursor_fetch(const TcParams& p, const Smem& s, i
 #pragma unroll
     for (int i = 0; i < 4; ++i) va[i] = (in && c.arow[i]) ? __ldg(c.arow[i] + c.kb * p.a_cs) : 1.0f;
     v0 = in ? __ldg(c.bs0 + c.kb) : 1.0f;
-    v1 = (in && kUp) ? __ldg(c.bs1 + c.kb) : 1.0f;
+    v1 = (in && F8<kUp>::N == 256) ? __ldg(c.bs1 + c.kb) : 1.0f;
 #pragma unroll
     for (int k = 0; k < kF8Stagers; ++k) cursor_next<kUp>(p, s, total, c);
 }
@@ -592,7 +597,7 @@ __device__ void scale_stager_f8(const TcParams& p, const Smem& s, int total, int
             sf[lane] = make_uint4(ue8m0x4(ca[j][0]), ue8m0x4(ca[j][1]), ue8m0x4(ca[j][2]), ue8m0x4(ca[j][3]));
             const uint32_t w0 = ue8m0x4(c0[j]), w1 = ue8m0x4(c1[j]);
             sf[32 + lane] = make_uint4(w0, w0, w0, w0);
-            if (kUp) sf[64 + lane] = make_uint4(w1, w1, w1, w1);
+            if (G::N == 256) sf[64 + lane] = make_uint4(w1, w1, w1, w1);
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s.full[stage]);
@@ -634,7 +639,7 @@ __device__ void mma_issuer_f8(const TcParams& p, const Smem& s, int total, uint3
             const uint32_t sf = tmem_base + (uint32_t)(kSfCol + 16 * stage);
             tc::tmem_cp_32x128b_x4(sf, tc::desc_rows16(sf_smem));                // A: columns sf .. sf+3
             tc::tmem_cp_32x128b_x4(sf + 8, tc::desc_rows16(sf_smem + 512));       // B rows 0-127
-            if (kUp) tc::tmem_cp_32x128b_x4(sf + 12, tc::desc_rows16(sf_smem + 1024));  // B rows 128-255
+            if (G::N == 256) tc::tmem_cp_32x128b_x4(sf + 12, tc::desc_rows16(sf_smem + 1024));  // B rows 128-255
 #pragma unroll
             for (int kk = 0; kk < kF8BK / 32; ++kk)
                 tc::mma_mx_e4m3(d, tc::desc_sw128_kmajor(a_addr + kk * 32), tc::desc_sw128_kmajor(b_addr + kk * 32),
@@ -746,28 +751,25 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
                 if (half == 0) p.out_scale[(int64_t)t.nt * p.max_rows + row] = scalbnf(1.0f, se);
             }
         } else {
-            uint32_t a0[32], a1[32];  // columns 64*half .. +63 of the 128-wide tile
+            uint32_t a[4][32];  // columns 128*half .. +127 of the 256-wide tile
             if (busy) {
-                tc::tmem_ld32(tb + 64 * half, a0);
-                tc::tmem_ld32(tb + 64 * half + 32, a1);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tc::tmem_ld32(tb + 128 * half + 32 * c, a[c]);
                 tc::tmem_wait_ld();
             }
             release_acc(s, buf);
             if (valid) {
                 uint4* dst =
-                    reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.H + t.nt * G::N + 64 * half);
+                    reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.H + t.nt * G::N + 128 * half);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pack_bf16x2(__uint_as_float(a0[8 * i]), __uint_as_float(a0[8 * i + 1])),
-                                        pack_bf16x2(__uint_as_float(a0[8 * i + 2]), __uint_as_float(a0[8 * i + 3])),
-                                        pack_bf16x2(__uint_as_float(a0[8 * i + 4]), __uint_as_float(a0[8 * i + 5])),
-                                        pack_bf16x2(__uint_as_float(a0[8 * i + 6]), __uint_as_float(a0[8 * i + 7])));
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[4 + i] = make_uint4(pack_bf16x2(__uint_as_float(a1[8 * i]), __uint_as_float(a1[8 * i + 1])),
-                                            pack_bf16x2(__uint_as_float(a1[8 * i + 2]), __uint_as_float(a1[8 * i + 3])),
-                                            pack_bf16x2(__uint_as_float(a1[8 * i + 4]), __uint_as_float(a1[8 * i + 5])),
-                                            pack_bf16x2(__uint_as_float(a1[8 * i + 6]), __uint_as_float(a1[8 * i + 7])));
+                    for (int i = 0; i < 4; ++i)
+                        dst[4 * c + i] =
+                            make_uint4(pack_bf16x2(__uint_as_float(a[c][8 * i]), __uint_as_float(a[c][8 * i + 1])),
+                                       pack_bf16x2(__uint_as_float(a[c][8 * i + 2]), __uint_as_float(a[c][8 * i + 3])),
+                                       pack_bf16x2(__uint_as_float(a[c][8 * i + 4]), __uint_as_float(a[c][8 * i + 5])),
+                                       pack_bf16x2(__uint_as_float(a[c][8 * i + 6]), __uint_as_float(a[c][8 * i + 7])));
             }
         }
         if (++buf == G::AccBufs) {
