@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_c
 // stage's MMAs, which execute in order after it.
 // Epilogues: up forms h = silu(g) * u, finds the 1x128 group amax of its row with its
 // partner thread (the other half of the columns) through shared memory and stores h
-// as e4m3 with its power-of-two scale; down stores ye as bf16.  The up kernel's single
+// as e4m3 with its power-of-two scale; down stores ye as bf16.  Each kernel's single
 // accumulator is moved into registers and released before any of that arithmetic.
 
 __device__ __forceinline__ uint32_t ue8m0x4(float pow2) {  // the biased exponent, in all four bytes
@@ -457,7 +457,7 @@ __device__ __forceinline__ uint32_t ue8m0x4(float pow2) {  // the biased exponen
     return e * 0x01010101u;
 }
 
-// One thread: the stage's TMA loads (A box and one or two 128-row B boxes).
+// One thread: the stage's TMA loads (the A box and the tile's 256-row B box).
 template <bool kUp>
 __device__ void producer_f8(const TcParams& p, const Smem& s, int total) {
     using G = F8<kUp>;
