@@ -42,6 +42,11 @@ __device__ __forceinline__ float spec_sigmoid(float x) {
     return __fdiv_rn(1.0f, __fadd_rn(1.0f, spec_exp(-c)));
 }
 
+// A NaN score takes part in the selection as -inf: every comparison with NaN is false,
+// so without this a row of NaNs would select no expert at all.  Finite scores, the
+// only ones the gates are defined for, are unchanged.
+__device__ __forceinline__ float nan_to_neg_inf(float v) { return v != v ? -INFINITY : v; }
+
 // Warp arg-max: larger value wins, equal values -> smaller id.
 __device__ __forceinline__ void warp_argmax(float& v, int& id) {
 #pragma unroll
@@ -71,7 +76,7 @@ __global__ void __launch_bounds__(256) route_softmax_kernel(int T, int E, int k,
 #pragma unroll
         for (int i = 0; i < NPER; ++i) {
             int e = lane + 32 * i;
-            v[i] = e < E ? __ldg(l + e) : -INFINITY;
+            v[i] = e < E ? nan_to_neg_inf(__ldg(l + e)) : -INFINITY;
             if (e >= E) taken |= 1u << i;
             else m = fmaxf(m, v[i]);
         }
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(256) route_grouped_kernel(int T, int E, int k,
             int e = lane + 32 * i;
             if (e < E) {
                 float s = spec_sigmoid(__ldg(l + e));
-                c[i] = __fadd_rn(s, bias ? __ldg(bias + e) : 0.0f);
+                c[i] = nan_to_neg_inf(__fadd_rn(s, bias ? __ldg(bias + e) : 0.0f));
                 cs[e] = c[i];
             } else {
                 c[i] = -INFINITY;
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(256) route_grouped_kernel(int T, int E, int k,
             if (lane == j) my_id = bi;
         }
         float sj = 0.0f;
-        if (lane < k) sj = 1.0f / (1.0f + expf(-__ldg(l + my_id)));
+        if (lane < k) sj = 1.0f / (1.0f + expf(-__ldg(l + (my_id < E ? my_id : 0))));
         float sum = warp_sum(sj);
         if (lane < k) {
             ids[(size_t)t * k + lane] = my_id;

@@ -301,3 +301,23 @@ def test_plan_without_token_of_gives_the_same_plan():
     assert np.array_equal(counts.cpu().numpy(), ref["counts"])
     assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
     assert np.array_equal(slot_of.cpu().numpy(), ref["slot_of"])
+
+
+@pytest.mark.parametrize("wl", [W.QWEN3_DECODE.with_(T=64), W.DSV3.with_(T=64)], ids=lambda w: w.name)
+def test_route_nan_logits_give_valid_ids(wl):
+    """Rows of NaN logits (and partly NaN rows) still select k distinct experts in
+    [0, E): the gates rank a NaN as -inf, so no id can leave the range (the weights of
+    such rows are unspecified)."""
+    cfg = B.config_of(wl)
+    logits = synth.logits(wl.T, wl.num_experts, "uniform", 5)
+    logits[: wl.T // 2] = float("nan")
+    logits[wl.T // 2:, ::3] = float("nan")
+    ids = torch.full((wl.T, wl.top_k), -1, dtype=torch.int32, device=DEV)
+    w = torch.empty(wl.T, wl.top_k, dtype=torch.float32, device=DEV)
+    B.moe_route(cfg, wl.T, logits.to(DEV), None, ids, w)
+    torch.cuda.synchronize()
+    got = ids.cpu().numpy()
+    assert got.min() >= 0 and got.max() < wl.num_experts
+    assert all(len(set(r)) == wl.top_k for r in got.tolist())
+    # the partly-NaN rows choose among their finite logits
+    assert np.all(got[wl.T // 2:] % 3 != 0)
