@@ -1,11 +1,13 @@
 // C ABI of libmoe_gb300: argument validation, workspace layout and the
 // Dual-Batch Overlap schedule.  Every computing step runs in the kernels of this
 // library; this file only checks arguments and enqueues.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -36,6 +38,61 @@ const DeviceInfo& device_info() {
     }
     return cache[dev];
 }
+
+namespace {
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename F>
+F driver_fn(const char* name) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(f);
+}
+
+}  // namespace
+
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) {
+        int dev = 0;  // no context on this thread yet: make the device's primary context current
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return 0;
+        if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    }
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+cudaError_t ensure_max_dynamic_smem(const void* func, int bytes) {
+    struct Entry {
+        const void* func;
+        unsigned long long ctx;
+        int bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    const unsigned long long ctx = current_context_id();
+    std::lock_guard<std::mutex> lk(mu);
+    if (ctx != 0)
+        for (const Entry& e : done)
+            if (e.func == func && e.ctx == ctx && e.bytes >= bytes) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess && ctx != 0) done.push_back(Entry{func, ctx, bytes});
+    return err;
+}
+
+namespace {
+std::atomic<long long> g_inject_wait_ns{0};
+}  // namespace
+
+int64_t wait_injection_ns() { return g_inject_wait_ns.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -80,6 +137,12 @@ moe_status check_config(const moe_config* c) {
 using namespace moe;
 
 extern "C" {
+
+moe_status moe_debug_inject_wait(int32_t enable, int64_t timeout_ns) {
+    if (enable && timeout_ns <= 0) return MOE_ERR_INVALID_ARG;
+    g_inject_wait_ns.store(enable ? (long long)timeout_ns : 0, std::memory_order_relaxed);
+    return MOE_OK;
+}
 
 const char* moe_status_string(moe_status s) {
     switch (s) {

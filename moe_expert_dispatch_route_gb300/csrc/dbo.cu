@@ -173,6 +173,16 @@ struct moe_dbo_handle {
     int device;
 };
 
+namespace {
+// An enqueue failed after the comm stream was forked from the compute stream: join it
+// back anyway, so that the comm work already queued (which may still write the
+// caller's buffers) is ordered before later work on the compute stream and a capture
+// is not left with an unjoined fork.  Best effort: the call reports MOE_ERR_CUDA.
+void join_after_failure(moe_dbo_handle* h, cudaStream_t compute, cudaStream_t comm) {
+    if (cudaEventRecord(h->ev[kEvDone], comm) == cudaSuccess) cudaStreamWaitEvent(compute, h->ev[kEvDone], 0);
+}
+}  // namespace
+
 extern "C" {
 
 moe_status moe_dbo_create(moe_dbo_handle** out) {
@@ -256,6 +266,7 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
     cudaError_t ce = cudaMemsetAsync(err, 0, sizeof(int32_t), cs);
     if (ce != cudaSuccess) return MOE_ERR_CUDA;
 
+    bool forked = false;  // the comm stream has been forked from the compute stream
     for (const Op& op : make_schedule(two)) {
         cudaStream_t q = op.stream == 0 ? cs : ms;
         const int u = op.ub < 0 ? 0 : op.ub;
@@ -298,7 +309,7 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
             }
             case MOE_OP_FFN: {
                 FfnArgs fa{counts, offsets, L.rows, xe, xe_scale, a->w13, a->w13_scale, a->w2, a->w2_scale,
-                           ye, b + L.ffn, err, two && u == 1 ? 1 : 0, L.rows};
+                           ye, b + L.ffn, err, two && u == 1 ? 1 : 0, L.rows, (int64_t)Tu * (c.top_k + c.num_shared)};
                 ce = launch_ffn(c, fa, ffn_grid, q);
                 break;
             }
@@ -312,7 +323,9 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
             st = MOE_ERR_CUDA;
             break;
         }
+        if (op.op == MOE_OP_WAIT && op.ev == kEvStart) forked = true;
     }
+    if (st != MOE_OK && forked) join_after_failure(h, cs, ms);
     return st;
 }
 
@@ -405,6 +418,7 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
     if (cudaMemsetAsync(err, 0, sizeof(int32_t), cs) != cudaSuccess) return MOE_ERR_CUDA;
 
     int layer[2] = {-1, -1};  // current layer of each ubatch (advanced by its stand-in)
+    bool forked = false;      // the comm stream has been forked from the compute stream
     for (const Op& op : make_stack_schedule(L, two, event_before_yield != 0)) {
         cudaStream_t q = op.stream == 0 ? cs : ms;
         const int u = op.ub < 0 ? 0 : op.ub;
@@ -453,13 +467,18 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
                 break;
             case MOE_OP_FFN: {
                 FfnArgs fa{counts, offsets, U.rows, xe, xe_scale, a->w13[l], fp8 ? a->w13_scale[l] : nullptr, a->w2[l],
-                           fp8 ? a->w2_scale[l] : nullptr, ye, b + U.ffn, err, two && u == 1 ? 1 : 0, U.rows};
+                           fp8 ? a->w2_scale[l] : nullptr, ye, b + U.ffn, err, two && u == 1 ? 1 : 0, U.rows,
+                           (int64_t)Tu * (c.top_k + c.num_shared)};
                 ce = launch_ffn(c, fa, ffn_grid, q);
                 break;
             }
             case MOE_OP_COMBINE: ce = launch_combine(c, Tu, ye, wts, slot_of, xout, comm_grid, q, act); break;
         }
-        if (ce != cudaSuccess) return MOE_ERR_CUDA;
+        if (ce != cudaSuccess) {
+            if (forked) join_after_failure(h, cs, ms);
+            return MOE_ERR_CUDA;
+        }
+        if (op.op == MOE_OP_WAIT && op.ev == kEvStart) forked = true;
     }
     return MOE_OK;
 }

@@ -50,16 +50,11 @@ template <bool kFp8>
 static cudaError_t launch_fused(const moe_config& c, int T, const int32_t* ids, int capacity, int align,
                                 int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* err, const void* x,
                                 void* xe, float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st) {
-    static int configured_dev = -1;
     const int kk = c.top_k + c.num_shared;
     const size_t smem = 2 * (size_t)T * kk * sizeof(int);
-    const int dev = device_info().device;
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(plan_dispatch_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             2 * kPlanEntriesPerChunk * (int)sizeof(int));
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
-    }
+    // the static plan tables plus up to 32 KB of entries exceed the default 48 KB
+    cudaError_t e = ensure_max_dynamic_smem(plan_dispatch_kernel<kFp8>, 2 * kPlanEntriesPerChunk * (int)sizeof(int));
+    if (e != cudaSuccess) return e;
     const int nvec = kFp8 ? c.hidden / 8 : c.hidden * elt_bytes(c.dtype) / 16;
     const int nvec_io = c.hidden * io_bytes(c.dtype) / 16;
     const long items = (long)T * ((nvec_io + 127) / 128);

@@ -2,6 +2,7 @@
 // Arguments are already validated by the caller; each launcher only enqueues.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -18,6 +19,23 @@ struct DeviceInfo {
 const DeviceInfo& device_info();
 moe_status check_config(const moe_config* c);  // shape limits and row alignment
 bool aligned16(const void* p);
+
+// Identity of the CUDA context current on the calling thread: unique for the life of
+// the process (a device reset followed by a new context gives a new id); 0 when it
+// cannot be read.  Host-side caches of per-context state -- device addresses of module
+// variables, kernel attributes -- are keyed on it so that they never go stale.
+unsigned long long current_context_id();
+// Test hook (moe_debug_inject_wait): > 0 makes every expert-FFN kernel launched from
+// now on first wait this long on a barrier nothing arrives on, then report
+// MOE_ERR_TIMEOUT and skip its work; 0 = off (the default).
+int64_t wait_injection_ns();
+// Raises the dynamic shared memory limit of a kernel to `bytes`, once per context
+// (thread-safe); later calls in the same context return at once.
+cudaError_t ensure_max_dynamic_smem(const void* func, int bytes);
+template <typename... A>
+cudaError_t ensure_max_dynamic_smem(void (*kern)(A...), int bytes) {
+    return ensure_max_dynamic_smem(reinterpret_cast<const void*>(kern), bytes);
+}
 
 // route.cu
 cudaError_t launch_route(const moe_config& c, int T, const float* logits, const float* bias,
@@ -63,14 +81,25 @@ struct FfnArgs {
     int32_t* err;
     int reverse;     // walk experts in descending order (L2 reuse across ubatches)
     int64_t xs_cs;   // layout of xe_scale: 0 = row-major, else column-major with this column stride
+    int64_t rows_hint = 0;  // rows actually used (tokens x (k+S)) when known, else 0
 };
 cudaError_t launch_ffn(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
+
+// ffn_pair.cu: the same FFN on CTA pairs (tcgen05.mma.cta_group::2, 256 x 256 tiles),
+// chosen for bf16 batches averaging at least 128 rows per expert (MOE_FFN_TILE=pair /
+// single forces either family for any layer)
+bool ffn_pair_supported(const moe_config& c);
+bool ffn_pair_preferred(const moe_config& c, int64_t rows_hint);
+cudaError_t launch_ffn_pair(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
 
 // ffn_simt.cu: portable CUDA-core grouped GEMM (fp32 layers, and any layer on request)
 cudaError_t launch_ffn_simt(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
 
-// ffn_tc.cu: tcgen05 / TMEM / TMA grouped GEMM (bf16 layers)
+// ffn_tc.cu: tcgen05 / TMEM / TMA grouped GEMM, one CTA per tile (bf16 and fp8 layers)
 bool ffn_tc_supported(const moe_config& c);
+void* tma_encode_fn();  // cuTensorMapEncodeTiled from the driver, or null
+// 2-D K-major [rows][inner] tensor map, 128-byte swizzle, box = one 128-byte row x box_rows
+bool make_tma_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, bool fp8, int box_rows);
 cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
 // the stand-in for a layer's non-MoE compute in a stack: out = x + x . Wa^T (bf16)
 bool standin_tc_supported(const moe_config& c);

@@ -22,11 +22,16 @@ static __device__ __align__(256) int32_t g_plan_scratch[kNoAllocScratchInts];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int32_t* g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchAddr {
+    unsigned long long ctx;  // context the address was looked up in
+    int32_t* ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
-// Device address of g_plan_scratch on the current device.  The host-side name of
-// the array is only a stand-in, so the address is looked up once per device with
-// that device current.
+// Device address of g_plan_scratch in the context current on this thread.  The
+// host-side name of the array is only a stand-in, so the address is looked up with
+// the device current, once per context: a device reset followed by a new context
+// gets a fresh lookup instead of a stale address.
 int32_t* scratch_for_current_device(cudaError_t* err) {
     int dev = 0;
     *err = cudaGetDevice(&dev);
@@ -35,14 +40,15 @@ int32_t* scratch_for_current_device(cudaError_t* err) {
         *err = cudaErrorInvalidDevice;
         return nullptr;
     }
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch[dev].ptr || ctx == 0 || g_scratch[dev].ctx != ctx) {
         void* p = nullptr;
         *err = cudaGetSymbolAddress(&p, g_plan_scratch);
         if (*err != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+        g_scratch[dev] = ScratchAddr{ctx, static_cast<int32_t*>(p)};
     }
-    return g_scratch_ptr[dev];
+    return g_scratch[dev].ptr;
 }
 
 }  // namespace

@@ -41,34 +41,76 @@ def test_status_strings():
     assert B.moe_status_string(99) == "unknown status"
 
 
+class _Buffers:
+    """Pointers for the rejection tests.  With a GPU they point into one real, zeroed
+    device buffer large enough for every shape below (so that, if a host check ever
+    regressed, a kernel would touch valid memory and the status assertion would fail
+    instead of a kernel running on a made-up address); without one they are small
+    integers (no kernel can launch)."""
+
+    def __init__(self, nbytes=1 << 30):
+        import torch
+
+        self.t = None
+        if torch.cuda.is_available():
+            self.t = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+            self.base = self.t.data_ptr()
+        else:
+            self.base = 0
+        self.next = 1 << 20
+
+    def __call__(self, misalign=0):
+        """A distinct 16-byte aligned pointer (plus `misalign` bytes), 16 MB apart."""
+        p = self.base + self.next + misalign
+        self.next += 16 << 20
+        assert self.t is None or self.next <= self.t.numel()
+        return p
+
+    def handle(self):
+        return ctypes.c_void_p(B.moe_dbo_create()) if self.t is not None else ctypes.c_void_p(1)
+
+    def close(self, h):
+        if self.t is not None:
+            B.moe_dbo_destroy(h.value)
+
+
 def test_invalid_arguments_rejected_on_host():
     L = B.lib()
+    P = _Buffers()
     cfg = B.config_of(W.QWEN3_DECODE)
     bad = B.config_of(W.QWEN3_DECODE)
     bad.top_k = 0
-    assert L.moe_route(ctypes.byref(bad), 4, 16, None, 16, 16, 0, None) == 1
-    assert L.moe_route(ctypes.byref(cfg), 4, None, None, 16, 16, 0, None) == 1
+    assert L.moe_route(ctypes.byref(bad), 4, P(), None, P(), P(), 0, None) == 1
+    assert L.moe_route(ctypes.byref(cfg), 4, None, None, P(), P(), 0, None) == 1
     assert L.moe_route(ctypes.byref(cfg), 0, None, None, None, None, 0, None) == 0  # empty batch
-    assert L.moe_dispatch(ctypes.byref(cfg), 4, 8, 16, 16, None, 0, 0, None) == 3     # misaligned x
-    assert L.moe_dispatch(ctypes.byref(cfg), 4, 16, 16, 16, None, -1, 0, None) == 1   # negative scale ld
+    assert L.moe_dispatch(ctypes.byref(cfg), 4, P(8), P(), P(), None, 0, 0, None) == 3     # misaligned x
+    assert L.moe_dispatch(ctypes.byref(cfg), 4, P(), P(), P(), None, -1, 0, None) == 1     # negative scale ld
     g = B.config_of(W.DSV3)
     g.n_group = 7  # 256 % 7 != 0
-    assert L.moe_route(ctypes.byref(g), 4, 16, None, 16, 16, 0, None) == 1
+    assert L.moe_route(ctypes.byref(g), 4, P(), None, P(), P(), 0, None) == 1
     f = B.config_of(W.QWEN3_PREFILL)
     f.hidden = 2000  # fp8 needs multiples of 128
-    assert L.moe_dispatch(ctypes.byref(f), 4, 16, 16, 16, 16, 0, 0, None) == 3
+    assert L.moe_dispatch(ctypes.byref(f), 4, P(), P(), P(), P(), 0, 0, None) == 3
     # expert FFN: a column-major scale stride must cover max_rows (and not be negative)
-    ffn = lambda ld: L.moe_expert_ffn(ctypes.byref(f8), 16, 16, 100, 16, 16, ld, 16, 16, 16, 16, 16, 16, 1 << 30,
-                                      None, 0, None)
     f8 = B.config_of(W.QWEN3_PREFILL)
+    ffn = lambda ld: L.moe_expert_ffn(ctypes.byref(f8), P(), P(), 100, P(), P(), ld, P(), P(), P(), P(), P(), P(),
+                                      1 << 20, None, 0, None)
     assert ffn(5) == 1 and ffn(-1) == 1
-    # plan: workspace required when the batch spans several chunks
+    # plan: workspace required when the batch spans several chunks (ids / slots of
+    # 100000 tokens would not fit the test buffer: the call must return first)
     assert B.moe_plan_workspace_size(cfg, 100000) > 0
-    assert L.moe_plan(ctypes.byref(cfg), 100000, 16, 0, 128, 16, 16, 16, 16, 16, None, 0, 0, None) == 4
-    # layer: workspace too small
-    h = ctypes.c_void_p(1)
-    args = B.MoeLayerArgs(16, None, 16, 16, None, 16, None, 16, 16, 16, None, 256, 1024)
-    assert L.moe_layer_dbo(h, ctypes.byref(cfg), ctypes.byref(args), 256, 0, 4, 0, 128, 0, None, None) == 4
+    assert L.moe_plan(ctypes.byref(cfg), 100000, P(), 0, 128, P(), P(), P(), P(), P(), None, 0, 0, None) == 4
+    # layer: workspace too small (the tiny layer: every buffer fits a 16 MB slot)
+    tiny = B.config_of(W.TINY)
+    h = P.handle()
+    args = B.MoeLayerArgs(P(), None, P(), P(), None, P(), None, P(), P(), P(), None, P(), 1024)
+    assert L.moe_layer_dbo(h, ctypes.byref(tiny), ctypes.byref(args), 64, 0, 4, 0, 128, 0, None, None) == 4
+    P.close(h)
+    if P.t is not None:  # nothing was written
+        import torch
+
+        torch.cuda.synchronize()
+        assert int(P.t.count_nonzero().item()) == 0
 
 
 def test_plan_rows_and_workspace_sizes():
