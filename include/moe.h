@@ -112,7 +112,9 @@ typedef struct {
  *     (equal -> lower group id); the k best c inside them are chosen (equal -> lower
  *     id); w = sigmoid(l) of the chosen (no bias), / their sum if renormalize, times
  *     routed_scale.  Selection is bit-reproducible; weights are fp32.
- * logits   device fp32 [T][E], row-major.
+ * logits   device fp32 [T][E], row-major.  The gates are defined for finite logits;
+ *          a NaN logit (or score) is ranked as -inf, so every id written is in [0, E)
+ *          whatever the input holds (the weights of such a row are unspecified).
  * bias     device fp32 [E] or NULL (grouped gate only; NULL = 0).
  * topk_ids device int32 [T][k] (out), descending score order.
  * topk_w   device fp32 [T][k] (out).
@@ -165,7 +167,9 @@ MOE_API moe_status moe_plan(const moe_config* cfg, int32_t T, const int32_t* top
  * entries is cut into chunks of about 1024; a smaller one needs no scratch); a larger T returns
  * MOE_ERR_WORKSPACE before anything is enqueued (MOE_DEBUG=1 prints why).
  * The first call on a device that needs the scratch looks up the array's device
- * address with that device current; make that first call before any stream capture.
+ * address with that device current (and so does the first such call in a new context
+ * of the device, e.g. after cudaDeviceReset); make that first call before any stream
+ * capture.
  * All calls share the one array, so calls whose kernels overlap on the GPU (on
  * different streams without ordering) race; calls ordered on one stream do not.
  * The array keeps the last call's contents; every entry a call reads is written
@@ -337,6 +341,17 @@ MOE_API int32_t moe_stack_schedule(int32_t layers, int32_t two_ubatches, int32_t
                                    int32_t* ops, int32_t max_ops);
 
 MOE_API const char* moe_status_string(moe_status s);
+
+/* ---------------------------------------------------------------------------
+ * moe_debug_inject_wait -- test hook for the failure path of the bounded device
+ * waits (the pages have no counterpart).  With enable != 0, every expert-FFN kernel
+ * launched afterwards (by moe_expert_ffn, moe_layer_dbo or moe_stack_dbo) begins with a
+ * wait, limited to timeout_ns, on a barrier that nothing ever completes, before it
+ * issues any copy: the wait runs out, the kernel stores MOE_ERR_TIMEOUT in err_flag,
+ * skips its work, frees its tensor memory and returns normally, so the context stays
+ * usable.  enable = 0 (the default) turns it off.  Process-wide, host-side only;
+ * enable != 0 with timeout_ns <= 0 is MOE_ERR_INVALID_ARG. */
+MOE_API moe_status moe_debug_inject_wait(int32_t enable, int64_t timeout_ns);
 
 #ifdef __cplusplus
 }

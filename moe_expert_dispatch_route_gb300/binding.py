@@ -91,6 +91,7 @@ _SIGS = {
                              _I32, _P, _P]),
     "moe_stack_schedule": (_I32, [_I32, _I32, _I32, _P, _I32]),
     "moe_status_string": (ctypes.c_char_p, [_I32]),
+    "moe_debug_inject_wait": (_I32, [_I32, _I64]),
 }
 EXPORTS = tuple(_SIGS)
 
@@ -219,6 +220,11 @@ def moe_dbo_schedule(two_ubatches: bool):
     buf = (ctypes.c_int32 * (4 * n))()
     lib().moe_dbo_schedule(int(two_ubatches), buf, n)
     return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
+
+
+def moe_debug_inject_wait(enable: bool, timeout_ns: int = 0):
+    """Test hook: FFN kernels launched while enabled let a bounded wait run out (see moe.h)."""
+    _check(lib().moe_debug_inject_wait(int(enable), int(timeout_ns)), "moe_debug_inject_wait")
 
 
 def moe_status_string(st: int) -> str:

@@ -25,8 +25,20 @@ static bool force_simt() {
     return v == 1;
 }
 
+// Rows the batch really uses: the caller's hint, else max_rows less the largest padding
+// an exact layout with 128-row alignment adds.
+static int64_t rows_estimate(const moe_config& c, const FfnArgs& a) {
+    if (a.rows_hint > 0) return a.rows_hint;
+    const int64_t pad = (int64_t)(c.num_experts + c.num_shared) * 127;
+    return a.max_rows > pad ? a.max_rows - pad : 0;
+}
+
 cudaError_t launch_ffn(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st) {
-    if (!force_simt() && ffn_tc_supported(c)) return launch_ffn_tc(c, a, grid_cap, st);
+    if (!force_simt() && ffn_tc_supported(c)) {
+        // prefill-sized batches: 256 x 256 tiles on CTA pairs; decode: one CTA per tile
+        if (ffn_pair_preferred(c, rows_estimate(c, a))) return launch_ffn_pair(c, a, grid_cap, st);
+        return launch_ffn_tc(c, a, grid_cap, st);
+    }
     return launch_ffn_simt(c, a, grid_cap, st);
 }
 

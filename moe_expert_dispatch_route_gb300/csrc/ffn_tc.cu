@@ -60,7 +60,7 @@ struct F8 {
 constexpr int kSfCol = 256;
 constexpr int kSfStageBytes = 1536;  // A scales, B scales of rows 0-127, of rows 128-255 (512 B each)
 constexpr int kMaxStages = 6;
-constexpr int kNumBars = 2 * kMaxStages + 2 + 2 + 1;  // full, empty, tmem full, tmem empty, drain
+constexpr int kNumBars = 2 * kMaxStages + 2 + 2 + 2;  // full, empty, tmem full, tmem empty, drain, never
 constexpr size_t kSmemTail =
     kNumBars * 8 + 16 + 3 * (kMaxExperts + 1) * sizeof(int) + 512 * sizeof(float) + 256 * sizeof(int);
 constexpr size_t smem_bytes(int stages, int stage_bytes, int sf_bytes) {
@@ -102,6 +102,7 @@ struct TcParams {
     float* out_scale;      // fp8 up: scales of the quantised h, column-major [I/128][max_rows]
     int dense_rows;        // counts == nullptr: one dense matrix of this many rows
     const void* resid;     // bf16 down: added to the product before rounding ([rows][H])
+    int64_t inject_ns;     // test hook: > 0 = the producer's first wait runs out after this long
 };
 
 struct Smem {
@@ -112,6 +113,7 @@ struct Smem {
     uint64_t* tfull;
     uint64_t* tempty;
     uint64_t* drain;
+    uint64_t* never;  // test hook: a barrier nothing ever arrives on
     uint32_t* tmem_base;
     volatile int* abort;
     int* tstart;
@@ -133,7 +135,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int stages, int stage_bytes,
     s.tfull = s.empty + stages;
     s.tempty = s.tfull + 2;
     s.drain = s.tempty + 2;
-    s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.never = s.drain + 1;
+    s.tmem_base = reinterpret_cast<uint32_t*>(s.drain + 2);
     s.abort = reinterpret_cast<volatile int*>(s.tmem_base + 1);
     s.tstart = reinterpret_cast<int*>(s.tmem_base + 4);
     s.cnt = s.tstart + (kMaxExperts + 1);
@@ -212,8 +215,19 @@ __device__ void scan_tiles(const TcParams& p, const Smem& s) {
 }
 
 // kKElems: elements per k-block (one 128-byte swizzle row): 64 bf16 or 128 e4m3.
+// The failure-path test hook: the producer's first wait (on a barrier nothing arrives
+// on) runs out before it issues any copy; the CTA reports MOE_ERR_TIMEOUT and every
+// role leaves through its abort check.
+__device__ __forceinline__ bool injected_failure(const TcParams& p, const Smem& s) {
+    if (p.inject_ns <= 0) return false;
+    tc::wait_on_nothing(s.never, (uint64_t)p.inject_ns);
+    fail(s, p.err);
+    return true;
+}
+
 template <bool kUp, int kKElems>
 __device__ void producer(const TcParams& p, const Smem& s, int total) {
+    if (injected_failure(p, s)) return;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t pending = 0, pend_par = 0;  // per stage: a load in flight, and its phase parity
@@ -400,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_c
             tc::mbar_init(&s.tempty[i], 4);
         }
         tc::mbar_init(s.drain, 1);
+        tc::mbar_init(s.never, 1);
         *s.abort = 0;
         tc::fence_barrier_init();
         for (int i = 0; i < kNumABoxes; ++i) tc::prefetch_tmap(&p.tmA[i]);
@@ -461,6 +476,7 @@ __device__ __forceinline__ uint32_t ue8m0x4(float pow2) {  // the biased exponen
 template <bool kUp>
 __device__ void producer_f8(const TcParams& p, const Smem& s, int total) {
     using G = F8<kUp>;
+    if (injected_failure(p, s)) return;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t pending = 0, pend_par = 0;
@@ -796,6 +812,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_
             tc::mbar_init(&s.tempty[i], 8);
         }
         tc::mbar_init(s.drain, 1);
+        tc::mbar_init(s.never, 1);
         *s.abort = 0;
         tc::fence_barrier_init();
         for (int i = 0; i < kNumABoxes; ++i) tc::prefetch_tmap(&p.tmA[i]);
@@ -833,32 +850,10 @@ __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-    return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encode_fn()); }
 
-// 2-D K-major matrix [rows][inner] with the 128-byte swizzle and a box of one
-// 128-byte row (64 bf16 or 128 e4m3) by box_rows rows.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, bool fp8, int box_rows = 128) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    const uint64_t elt = fp8 ? 1 : 2;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * elt};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return make_tma_map_2d(m, base, inner, rows, fp8, box_rows);
 }
 
 // W13 [NE][2I][K] as a 3-D tensor [2 NE][I][K] (gate half 2e, up half 2e + 1) with a
@@ -878,15 +873,10 @@ bool make_map_w13(CUtensorMap* m, const void* base, uint64_t K, uint64_t I, uint
 
 template <bool kUp, bool kFp8>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
-    static int configured_dev = -1;
-    const int dev = device_info().device;
     auto kern = kFp8 ? ffn_tc_fp8_kernel<kUp> : ffn_tc_bf16_kernel<kUp>;
     const size_t smem = kFp8 ? kF8SmemBytes<kUp> : kSmemBytes;
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
-    }
+    cudaError_t e = ensure_max_dynamic_smem(kern, (int)smem);
+    if (e != cudaSuccess) return e;
     // programmatic dependent launch: this kernel's prologue may overlap the tail of the
     // previous kernel on the stream; it waits (griddepcontrol.wait) before reading
     // anything that kernel wrote
@@ -904,6 +894,34 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
 }
 
 }  // namespace
+
+void* tma_encode_fn() {
+    static void* fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = f;
+    }
+    return fn;
+}
+
+// 2-D K-major matrix [rows][inner] with the 128-byte swizzle and a box of one
+// 128-byte row (64 bf16 or 128 e4m3) by box_rows rows.
+bool make_tma_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, bool fp8, int box_rows) {
+    auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encode_fn());
+    if (!enc) return false;
+    const uint64_t elt = fp8 ? 1 : 2;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * elt};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool ffn_tc_supported(const moe_config& c) {
     const DeviceInfo& d = device_info();
@@ -948,6 +966,7 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     up.a_cs = a.xs_cs ? a.xs_cs : 1;
     up.b_scale = a.w13_scale;
     up.out_scale = h_scale;
+    up.inject_ns = wait_injection_ns();
     TcParams dn = up;
     for (int i = 0; i < kNumABoxes; ++i)
         if (!make_map(&dn.tmA[i], h, (uint64_t)I, (uint64_t)a.max_rows, fp8, a_box_rows(i)))
