@@ -198,16 +198,21 @@ def max_over_ranks(v: float, world: int) -> float:
 
 def launches_per_step(wl, split_two: bool) -> int:
     """Kernels this library launches for one layer call, per ubatch: route; plan and
-    dispatch (one fused kernel when the plan is a single chunk); the two FFN kernels;
-    combine."""
+    dispatch (one fused kernel when the plan is a single chunk; route, plan and dispatch
+    in one clustered kernel for a small batch that runs alone: the unsplit batch or
+    ubatch 0); the two FFN kernels; combine."""
     kk = wl.top_k + wl.num_shared
     tpc = max(1, 4096 // kk)
     sizes = [wl.split, wl.T - wl.split] if split_two else [wl.T]
     n = 0
-    for Tu in sizes:
+    for u, Tu in enumerate(sizes):
         chunks = max(1, math.ceil(Tu / tpc))
-        # route, (plan + dispatch fused | plan count + plan assign + dispatch), 2 FFN kernels, combine
-        n += 1 + (1 if chunks == 1 else 3) + 2 + 1
+        alone = u == 0
+        if chunks == 1 and alone and Tu <= 128:
+            head = 1
+        else:
+            head = 1 + (1 if chunks == 1 else 3)  # route + (plan/dispatch fused | count, assign, dispatch)
+        n += head + 2 + 1
     return n
 
 

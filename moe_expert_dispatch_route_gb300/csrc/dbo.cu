@@ -284,15 +284,27 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
         const bool overlapped = (u == 1 && op.op != MOE_OP_COMBINE) || (u == 0 && op.op == MOE_OP_COMBINE);
         const int comm_grid = (two && overlapped) ? comm_cap : sms * 8;
         const int ffn_grid = two ? ffn_cap : sms * 8;
+        // the clustered head (clusters of up to 8 CTAs) only where nothing else runs: beside
+        // an FFN the free SMs are scattered over the GPCs and a cluster might not fit
+        const bool cluster_head = !(two && overlapped) && head_fusable(c, Tu);
         const float* logits_u = a->logits + (size_t)t0[u] * c.num_experts;
         int32_t* ids_u = a->topk_ids + (size_t)t0[u] * k;
         float* w_u = a->topk_w + (size_t)t0[u] * k;
         switch (op.op) {
             case MOE_OP_RECORD: ce = cudaEventRecord(h->ev[op.ev], q); break;
             case MOE_OP_WAIT: ce = cudaStreamWaitEvent(q, h->ev[op.ev], 0); break;
-            case MOE_OP_ROUTE: ce = launch_route(c, Tu, logits_u, a->bias, ids_u, w_u, comm_grid, q); break;
+            case MOE_OP_ROUTE:
+                if (cluster_head) {  // small batch running alone: route, plan and dispatch in one launch
+                    const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
+                    ce = launch_route_plan_dispatch(c, Tu, logits_u, a->bias, ids_u, w_u, capacity, align, counts,
+                                                    offsets, slot_of, err, xu, xe, xe_scale, L.rows, comm_grid, q);
+                } else {
+                    ce = launch_route(c, Tu, logits_u, a->bias, ids_u, w_u, comm_grid, q);
+                }
+                break;
             case MOE_OP_PLAN:
-                if (plan_dispatch_fusable(c, Tu)) {  // small batch: plan and dispatch in one launch
+                if (cluster_head) break;             // done with the route
+                if (plan_dispatch_fusable(c, Tu)) {  // single-chunk batch: plan and dispatch in one launch
                     const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
                     ce = launch_plan_dispatch(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, err, xu, xe,
                                               xe_scale, L.rows, comm_grid, q);

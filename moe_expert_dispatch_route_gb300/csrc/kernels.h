@@ -48,8 +48,14 @@ cudaError_t launch_plan(const moe_config& c, int T, const int32_t* ids, int capa
                         int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* token_of,
                         int32_t* err, int32_t* hist_ws, int grid_cap, cudaStream_t st);
 
-// head.cu: plan + dispatch in one launch when the plan is a single chunk
+// head.cu: plan + dispatch in one launch when the plan is a single chunk; route + plan +
+// dispatch in one launch (thread-block clusters) when, in addition, the batch is small
 bool plan_dispatch_fusable(const moe_config& c, int T);
+bool head_fusable(const moe_config& c, int T);
+cudaError_t launch_route_plan_dispatch(const moe_config& c, int T, const float* logits, const float* bias,
+                                       int32_t* ids, float* w, int capacity, int align, int32_t* counts,
+                                       int32_t* offsets, int32_t* slot_of, int32_t* err, const void* x, void* xe,
+                                       float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st);
 cudaError_t launch_plan_dispatch(const moe_config& c, int T, const int32_t* ids, int capacity, int align,
                                  int32_t* counts, int32_t* offsets, int32_t* slot_of, int32_t* err, const void* x,
                                  void* xe, float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st);

@@ -11,10 +11,12 @@ constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kPlanEntriesPerChunk = 4096;       // a batch up to this many entries is one chunk
 constexpr int kPlanEntriesPerChunkMulti = 1024;  // larger batches: chunks of about this many
 
-// Expert of entry (t, j); -1 for a routed id outside [0, E).
+// Expert of entry (t, j); -1 for a routed id outside [0, E).  kSharedIds: ids are in
+// shared memory (the fused head), else in global memory.
+template <bool kSharedIds = false>
 __device__ __forceinline__ int entry_expert(const int32_t* ids, int t, int j, int k, int E) {
     if (j >= k) return E + (j - k);
-    int e = __ldg(ids + (size_t)t * k + j);
+    int e = kSharedIds ? ids[(size_t)t * k + j] : __ldg(ids + (size_t)t * k + j);
     return (e >= 0 && e < E) ? e : -1;
 }
 
@@ -58,11 +60,13 @@ __device__ __forceinline__ void block_exclusive_scan(const int* v, int* out, int
     __syncthreads();
 }
 
-// One CTA's share of the plan: chunk `chunk` of `nchunks`.  chunk_e: shared memory for
+// One CTA's share of the plan: chunk `chunk` of `nchunks` (ids in shared memory when
+// kSharedIds).  chunk_e: shared memory for
 // the chunk's entry experts.  write_outputs: this CTA stores counts / offsets (chunk 0),
 // slot_of and token_of; slot_sm (may be null): the chunk's slots are also kept in
 // shared memory (the fused plan + dispatch kernel, where every CTA plans the whole batch
 // and only CTA 0 writes).  Every thread of the CTA must call it.
+template <bool kSharedIds = false>
 __device__ __forceinline__ void plan_assign_cta(int T, int k, int S, int E, int tpc, int nchunks, int chunk,
                                                 int capacity, int align, const int32_t* __restrict__ ids,
                                                 const int32_t* __restrict__ hist, int32_t* __restrict__ counts,
@@ -90,12 +94,13 @@ __device__ __forceinline__ void plan_assign_cta(int T, int k, int S, int E, int 
         }
         __syncthreads();
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            int e = entry_expert(ids, t0 + i / kk, i % kk, k, E);
+            int e = entry_expert<kSharedIds>(ids, t0 + i / kk, i % kk, k, E);
             chunk_e[i] = e;
             if (e >= 0) atomicAdd(&total[e], 1);
         }
     } else {
-        for (int i = threadIdx.x; i < n; i += blockDim.x) chunk_e[i] = entry_expert(ids, t0 + i / kk, i % kk, k, E);
+        for (int i = threadIdx.x; i < n; i += blockDim.x)
+            chunk_e[i] = entry_expert<kSharedIds>(ids, t0 + i / kk, i % kk, k, E);
         for (int e = threadIdx.x; e < NE; e += blockDim.x) {
             int tot = 0, bef = 0;
             for (int c = 0; c < nchunks; ++c) {
