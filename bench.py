@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--capacity", type=int, default=None,
                     help="rows per expert per ubatch (worst-token layout); -1 = the ubatch size")
     ap.add_argument("--comm-sms", type=int, default=COMM_SMS)
+    ap.add_argument("--fused", default="none", choices=["none", "gather", "combine", "both"],
+                    help="time the layer with the gather fused into the expert GEMM and / or the combine into "
+                         "its epilogue; every other mode is timed beside it")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the DBO-gain and e2e legs")
     ap.add_argument("--stack", type=int, default=0,
@@ -196,7 +199,7 @@ def max_over_ranks(v: float, world: int) -> float:
     return float(t.item())
 
 
-def launches_per_step(wl, split_two: bool) -> int:
+def launches_per_step(wl, split_two: bool, fused: str = "none", tc: bool = True) -> int:
     """Kernels this library launches for one layer call, per ubatch: route; plan and
     dispatch (one fused kernel when the plan is a single chunk; route, plan and dispatch
     in one clustered kernel for a small batch that runs alone: the unsplit batch or
@@ -207,6 +210,12 @@ def launches_per_step(wl, split_two: bool) -> int:
     n = 0
     for u, Tu in enumerate(sizes):
         chunks = max(1, math.ceil(Tu / tpc))
+        if fused != "none" and tc:  # route, plan (count + assign when chunked), gather step, FFN, combine
+            gather = fused in ("gather", "both")
+            n += 1 + (1 if chunks == 1 else 2)
+            n += (1 if wl.dtype == "fp8" else 0) if gather else 1  # quantisation | dispatch
+            n += 2 + (0 if fused in ("combine", "both") else 1)
+            continue
         alone = u == 0
         if chunks == 1 and alone and Tu <= 128:
             head = 1
@@ -282,11 +291,15 @@ def run_ours(args, rank, world, local):
     compute = torch.cuda.Stream(device=dev)
     comm_sms = args.comm_sms
 
-    def enqueue(split=0, same=False, a=args_c, cs=None):
-        cs = cs or torch.cuda.current_stream()
-        B.moe_layer_dbo(handle, cfg, a, T, split, 4, cap, align, comm_sms, cs, cs if same else comm)
+    modes = {"none": 0, "gather": B.LAYER_FUSED_GATHER, "combine": B.LAYER_FUSED_COMBINE, "both": B.LAYER_FUSED}
+    flags = modes[args.fused]
 
-    def capture(**kw):
+    def enqueue(split=0, same=False, a=args_c, cs=None, fl=None):
+        cs = cs or torch.cuda.current_stream()
+        B.moe_layer_dbo_ex(handle, cfg, a, T, split, 4, cap, align, comm_sms, flags if fl is None else fl, cs,
+                           cs if same else comm)
+
+    def capture(**kw):  # split, same, a, fl
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(compute):
             enqueue(**kw)  # eager warm call (also builds any per-device state)
@@ -358,6 +371,18 @@ def run_ours(args, rank, world, local):
                       "gain_vs_two_ubatches_one_stream": round(ms_serial / ms, 4),
                       "gain_vs_unsplit": round(ms_unsplit / ms, 4), "comm_sms": comm_sms}
         del g_serial, g_unsplit
+        # the other modes: the gather fused into the expert GEMM and / or the combine into its
+        # epilogue, against dispatched rows and the combine kernel
+        times = {args.fused: ms}
+        for name, fl in modes.items():
+            if name not in times and wl.dtype != "f32":
+                g_other = capture(split=0, fl=fl)
+                times[name] = max_over_ranks(time_graph(g_other, args.steps, args.warmup), world)
+                del g_other
+        if len(times) > 1:
+            res["fused"] = {"timed_mode": args.fused, "ms": {k: round(v, 5) for k, v in times.items()},
+                            "gain_vs_unfused": {k: round(times["none"] / v, 4) for k, v in times.items()},
+                            "bytes_saved_by_gather_per_step": fused_bytes_saved(wl, two)}
 
     # ---- roofline of the dominant kernel: moe_expert_ffn on ubatch 0, timed alone
     roof = ffn_roofline(B, wl, cfg, inp, dev, args, comm_sms, compute)
@@ -375,12 +400,14 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "fp8e4m3"}[wl.dtype],
         "data": "synthetic (seeded N(0,1) logits / hidden states, N(0,0.02) weights)",
-        "config": {"workload": wl.describe(), "T": T, "hidden": H, "inter": wl.inter, "experts": E,
+        "config": {"workload": wl.describe() + ("" if args.fused == "none" else f" fused-{args.fused}"), "T": T,
+                   "hidden": H,
+                   "inter": wl.inter, "experts": E,
                    "shared": wl.num_shared, "top_k": k, "ubatches": 2 if two else 1, "split": wl.split,
                    "layout": f"capacity {cap}" if cap else f"exact, align {align}", "comm_sms": comm_sms,
                    "graph": "CUDA graph replay", "l2": "inputs larger than L2 (expert weights "
                    f"{weights_bytes(wl) / 1e9:.2f} GB > 129 MB L2)", "parallelism": f"replicas x{world}"},
-        "gpu_launches": launches_per_step(wl, two) * args.steps * n_blocks,
+        "gpu_launches": launches_per_step(wl, two, args.fused, wl.dtype != "f32") * args.steps * n_blocks,
         "timing": timing,
         "clocks": clocks,
         "roofline": roof,
@@ -466,6 +493,24 @@ def run_stack(args, rank, world, local):
                      "gain_of_event_before_yield": round(ms_old / ms_fix, 4),
                      "ms_unsplit": round(ms_unsplit, 5), "gain_vs_unsplit": round(ms_unsplit / ms_fix, 4)}}
     return out
+
+
+def fused_bytes_saved(wl, two: bool) -> dict:
+    """DRAM bytes the fused layer does not move, per step (model): dispatch's reads of x
+    and writes of xe (+ scales), the gate/up kernel's reads of xe, and the combine's
+    re-reads of ye; it adds the per-token quantisation of x for fp8 (reads x, writes x_q),
+    the gathers' reads of x / x_q (once per token: the rows of a ubatch stay in L2) and the
+    combine's reads of ye inside the down kernel (counted the same as the kernel's)."""
+    T, H, kk = wl.T, wl.hidden, wl.top_k + wl.num_shared
+    io, elt = (4, 4) if wl.dtype == "f32" else (2, 2 if wl.dtype == "bf16" else 1)
+    rows = T * kk
+    scales = rows * (H // 128) * 4 if wl.dtype == "fp8" else 0
+    dispatch = T * H * io + rows * H * elt + scales
+    xe_read = rows * H * elt + scales
+    fused_in = (T * H * io + T * H * elt + T * (H // 128) * 4 if wl.dtype == "fp8" else 0) + T * H * elt
+    return {"model_bytes": int(dispatch + xe_read - fused_in),
+            "note": "dispatch (x read, xe written) + xe read by the gate/up GEMM, less the per-token quantisation "
+                    "and one gathered read of x per token"}
 
 
 def weights_bytes(wl) -> float:

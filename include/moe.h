@@ -285,6 +285,27 @@ MOE_API moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const
                          int32_t T, int32_t split, int32_t min_tokens, int32_t capacity,
                          int32_t align, int32_t comm_sms, moe_stream_t compute, moe_stream_t comm);
 
+/* moe_layer_dbo_ex -- moe_layer_dbo with options: the exchange around the experts fused
+ * into the grouped GEMM ("DeepEP HT: full decode CUDA graphs via worst-token dispatch",
+ * description: dispatch and combine around the experts).  flags (either or both):
+ *   MOE_LAYER_FUSED_GATHER  the plan also records the token of every row, and the
+ *     gate/up kernel takes each A row straight from x by that token (TMA gather of 4 rows
+ *     at a time) instead of from a dispatched copy; fp8 layers quantise each token's row
+ *     once instead of once per chosen expert.
+ *   MOE_LAYER_FUSED_COMBINE  the down kernel's epilogue stores ye and the last of a
+ *     token's k+S rows to finish a slab of 128 columns (256 for bf16) forms that slab of
+ *     y in the fixed (j, then s) order of moe_combine; there is no combine step.  With an
+ *     entry dropped by a capacity overflow (MOE_ERR_CAPACITY) its token's y row is left
+ *     unwritten in this mode.
+ * No float atomics: the result is the same, bit for bit, as the unfused layer.  Served by
+ * the tensor-core FFN (bf16 and fp8 layers); other layers (fp32, or the CUDA-core FFN
+ * forced) run unfused.  Other bits: MOE_ERR_INVALID_ARG.  flags = 0 is moe_layer_dbo. */
+enum { MOE_LAYER_FUSED_GATHER = 1, MOE_LAYER_FUSED_COMBINE = 2, MOE_LAYER_FUSED = 3 };
+MOE_API moe_status moe_layer_dbo_ex(moe_dbo_handle* h, const moe_config* cfg, const moe_layer_args* args,
+                                    int32_t T, int32_t split, int32_t min_tokens, int32_t capacity,
+                                    int32_t align, int32_t comm_sms, int32_t flags, moe_stream_t compute,
+                                    moe_stream_t comm);
+
 /* The enqueue schedule moe_layer_dbo follows, for inspection (host only, no GPU
  * needed).  Writes up to max_ops records of 4 int32 each: {stream (0 compute,
  * 1 comm), op (see MOE_OP_*), ubatch (0/1, -1 = none), event id (record/wait) or -1}
@@ -300,6 +321,8 @@ enum {
     MOE_OP_STANDIN = 7
 };
 MOE_API int32_t moe_dbo_schedule(int32_t two_ubatches, int32_t* ops, int32_t max_ops);
+/* The schedule of moe_layer_dbo_ex with these flags (MOE_LAYER_FUSED_COMBINE: no combine step). */
+MOE_API int32_t moe_dbo_schedule_ex(int32_t two_ubatches, int32_t flags, int32_t* ops, int32_t max_ops);
 
 /* ---------------------------------------------------------------------------
  * A stack of L layers with Dual-Batch Overlap across layer boundaries.  The pages'

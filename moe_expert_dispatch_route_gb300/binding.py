@@ -86,6 +86,9 @@ _SIGS = {
     "moe_layer_dbo": (_I32, [_P, _CFG, ctypes.POINTER(MoeLayerArgs), _I32, _I32, _I32, _I32, _I32, _I32,
                              _P, _P]),
     "moe_dbo_schedule": (_I32, [_I32, _P, _I32]),
+    "moe_layer_dbo_ex": (_I32, [_P, _CFG, ctypes.POINTER(MoeLayerArgs), _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                                _P, _P]),
+    "moe_dbo_schedule_ex": (_I32, [_I32, _I32, _P, _I32]),
     "moe_stack_workspace_size": (_SZ, [_CFG, _I32, _I32, _I32]),
     "moe_stack_dbo": (_I32, [_P, _CFG, ctypes.POINTER(MoeStackArgs), _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                              _I32, _P, _P]),
@@ -215,10 +218,21 @@ def moe_layer_dbo(handle, cfg, args: MoeLayerArgs, T, split=0, min_tokens=4, cap
                                align, comm_sms, cs, ms), "moe_layer_dbo")
 
 
-def moe_dbo_schedule(two_ubatches: bool):
-    n = lib().moe_dbo_schedule(int(two_ubatches), None, 0)
+LAYER_FUSED_GATHER, LAYER_FUSED_COMBINE, LAYER_FUSED = 1, 2, 3
+
+
+def moe_layer_dbo_ex(handle, cfg, args: MoeLayerArgs, T, split=0, min_tokens=4, capacity=0, align=128,
+                     comm_sms=0, flags=0, compute=None, comm=None):
+    cs = _stream(compute)
+    ms = _stream(comm) if comm is not None else cs
+    _check(lib().moe_layer_dbo_ex(handle, ctypes.byref(cfg), ctypes.byref(args), T, split, min_tokens, capacity,
+                                  align, comm_sms, flags, cs, ms), "moe_layer_dbo_ex")
+
+
+def moe_dbo_schedule(two_ubatches: bool, flags: int = 0):
+    n = lib().moe_dbo_schedule_ex(int(two_ubatches), flags, None, 0)
     buf = (ctypes.c_int32 * (4 * n))()
-    lib().moe_dbo_schedule(int(two_ubatches), buf, n)
+    lib().moe_dbo_schedule_ex(int(two_ubatches), flags, buf, n)
     return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
 
 

@@ -39,7 +39,10 @@ struct Op {
     int ev;      // event id for RECORD / WAIT, else -1
 };
 
-std::vector<Op> make_schedule(bool two) {
+// fused (the combine inside the expert FFN's down kernel): there is no combine step, so
+// a ubatch's comm side is route, plan (with token_of) and its DISPATCH step (the gather,
+// or with the gather fused too, for fp8 the per-token quantisation).
+std::vector<Op> make_schedule(bool two, bool fused = false) {
     std::vector<Op> s;
     auto add = [&](int st, int op, int ub, int ev) { s.push_back(Op{st, op, ub, ev}); };
     if (!two) {
@@ -47,7 +50,22 @@ std::vector<Op> make_schedule(bool two) {
         add(0, MOE_OP_PLAN, 0, -1);
         add(0, MOE_OP_DISPATCH, 0, -1);
         add(0, MOE_OP_FFN, 0, -1);
-        add(0, MOE_OP_COMBINE, 0, -1);
+        if (!fused) add(0, MOE_OP_COMBINE, 0, -1);
+        return s;
+    }
+    if (fused) {
+        add(0, MOE_OP_RECORD, -1, kEvStart);
+        add(1, MOE_OP_WAIT, -1, kEvStart);
+        for (int u = 0; u < 2; ++u) {
+            add(1, MOE_OP_ROUTE, u, -1);  // ubatch 1's overlaps the experts of ubatch 0
+            add(1, MOE_OP_PLAN, u, -1);
+            add(1, MOE_OP_DISPATCH, u, -1);
+            add(1, MOE_OP_RECORD, u, u ? kEvDisp1 : kEvDisp0);
+            add(0, MOE_OP_WAIT, u, u ? kEvDisp1 : kEvDisp0);
+            add(0, MOE_OP_FFN, u, -1);
+        }
+        add(1, MOE_OP_RECORD, -1, kEvDone);
+        add(0, MOE_OP_WAIT, -1, kEvDone);
         return s;
     }
     add(0, MOE_OP_RECORD, -1, kEvStart);  // fork: the comm stream starts after the inputs
@@ -135,7 +153,9 @@ std::vector<Op> make_stack_schedule(int L, bool two, bool before_yield) {
 
 // Byte layout of one ubatch's slice of the layer workspace.
 struct UbLayout {
-    size_t counts, offsets, slot_of, hist, xe, xe_scale, ye, ffn, total;
+    size_t counts, offsets, slot_of, hist, xe, xe_scale, ye, ffn;
+    size_t token_of, xq, xq_scale, comb_cnt;  // the fused gather / combine
+    size_t total;
     int64_t rows;
 };
 
@@ -159,6 +179,11 @@ UbLayout ub_layout(const moe_config& c, int T, int capacity, int align) {
     L.xe_scale = take(c.dtype == MOE_FP8_E4M3 ? (size_t)L.rows * (H / 128) * 4 : 0);
     L.ye = take((size_t)L.rows * H * io_bytes(c.dtype));
     L.ffn = take(ffn_scratch_bytes(c, L.rows));
+    const bool fp8 = c.dtype == MOE_FP8_E4M3;
+    L.token_of = take((size_t)L.rows * 4);
+    L.xq = take(fp8 ? (size_t)T * H : 0);
+    L.xq_scale = take(fp8 ? (size_t)T * (H / 128) * 4 : 0);
+    L.comb_cnt = take((size_t)T * (H / 128) * 4);
     L.total = o;
     return L;
 }
@@ -208,7 +233,11 @@ void moe_dbo_destroy(moe_dbo_handle* h) {
 }
 
 int32_t moe_dbo_schedule(int32_t two_ubatches, int32_t* ops, int32_t max_ops) {
-    std::vector<Op> s = make_schedule(two_ubatches != 0);
+    return moe_dbo_schedule_ex(two_ubatches, 0, ops, max_ops);
+}
+
+int32_t moe_dbo_schedule_ex(int32_t two_ubatches, int32_t flags, int32_t* ops, int32_t max_ops) {
+    std::vector<Op> s = make_schedule(two_ubatches != 0, (flags & MOE_LAYER_FUSED_COMBINE) != 0);
     if (ops)
         for (int i = 0; i < (int)s.size() && i < max_ops; ++i) {
             ops[4 * i + 0] = s[i].stream;
@@ -228,8 +257,15 @@ size_t moe_layer_workspace_size(const moe_config* cfg, int32_t T, int32_t capaci
 moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_layer_args* a, int32_t T,
                          int32_t split, int32_t min_tokens, int32_t capacity, int32_t align,
                          int32_t comm_sms, moe_stream_t compute_s, moe_stream_t comm_s) {
+    return moe_layer_dbo_ex(h, cfg, a, T, split, min_tokens, capacity, align, comm_sms, 0, compute_s, comm_s);
+}
+
+moe_status moe_layer_dbo_ex(moe_dbo_handle* h, const moe_config* cfg, const moe_layer_args* a, int32_t T,
+                            int32_t split, int32_t min_tokens, int32_t capacity, int32_t align, int32_t comm_sms,
+                            int32_t flags, moe_stream_t compute_s, moe_stream_t comm_s) {
     if (!h || !cfg || !a) return MOE_ERR_INVALID_ARG;
     if (T < 0 || split < 0 || capacity < 0 || align < 1 || comm_sms < 0) return MOE_ERR_INVALID_ARG;
+    if (flags & ~MOE_LAYER_FUSED) return MOE_ERR_INVALID_ARG;  // the two fusion bits only
     const moe_status cs_ok = check_config(cfg);
     if (cs_ok != MOE_OK) return cs_ok;
     if (T == 0) return MOE_OK;
@@ -266,8 +302,14 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
     cudaError_t ce = cudaMemsetAsync(err, 0, sizeof(int32_t), cs);
     if (ce != cudaSuccess) return MOE_ERR_CUDA;
 
+    // the fused gather / combine is served by the tensor-core FFN (bf16 and fp8 layers);
+    // other layers run the steps unfused
+    const bool tc = ffn_tc_selected(c);
+    const bool fgather = (flags & MOE_LAYER_FUSED_GATHER) && tc;
+    const bool fcombine = (flags & MOE_LAYER_FUSED_COMBINE) && tc;
+    const bool fused = fgather || fcombine;  // the plan records token_of
     bool forked = false;  // the comm stream has been forked from the compute stream
-    for (const Op& op : make_schedule(two)) {
+    for (const Op& op : make_schedule(two, fcombine)) {
         cudaStream_t q = op.stream == 0 ? cs : ms;
         const int u = op.ub < 0 ? 0 : op.ub;
         char* b = ub_base[u];
@@ -286,7 +328,11 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
         const int ffn_grid = two ? ffn_cap : sms * 8;
         // the clustered head (clusters of up to 8 CTAs) only where nothing else runs: beside
         // an FFN the free SMs are scattered over the GPCs and a cluster might not fit
-        const bool cluster_head = !(two && overlapped) && head_fusable(c, Tu);
+        const bool cluster_head = !fused && !(two && overlapped) && head_fusable(c, Tu);
+        int32_t* token_of = reinterpret_cast<int32_t*>(b + L.token_of);
+        const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
+        void* xq = b + L.xq;
+        float* xq_scale = reinterpret_cast<float*>(b + L.xq_scale);
         const float* logits_u = a->logits + (size_t)t0[u] * c.num_experts;
         int32_t* ids_u = a->topk_ids + (size_t)t0[u] * k;
         float* w_u = a->topk_w + (size_t)t0[u] * k;
@@ -295,7 +341,6 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
             case MOE_OP_WAIT: ce = cudaStreamWaitEvent(q, h->ev[op.ev], 0); break;
             case MOE_OP_ROUTE:
                 if (cluster_head) {  // small batch running alone: route, plan and dispatch in one launch
-                    const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
                     ce = launch_route_plan_dispatch(c, Tu, logits_u, a->bias, ids_u, w_u, capacity, align, counts,
                                                     offsets, slot_of, err, xu, xe, xe_scale, L.rows, comm_grid, q);
                 } else {
@@ -304,8 +349,12 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
                 break;
             case MOE_OP_PLAN:
                 if (cluster_head) break;             // done with the route
+                if (fused) {                         // the FFN gathers by token: token_of wanted
+                    ce = launch_plan(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, token_of, err,
+                                     reinterpret_cast<int32_t*>(b + L.hist), comm_grid, q);
+                    break;
+                }
                 if (plan_dispatch_fusable(c, Tu)) {  // single-chunk batch: plan and dispatch in one launch
-                    const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
                     ce = launch_plan_dispatch(c, Tu, ids_u, capacity, align, counts, offsets, slot_of, err, xu, xe,
                                               xe_scale, L.rows, comm_grid, q);
                 } else {
@@ -314,14 +363,35 @@ moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_lay
                 }
                 break;
             case MOE_OP_DISPATCH: {
-                if (plan_dispatch_fusable(c, Tu)) break;  // done with the plan
-                const char* xu = static_cast<const char*>(a->x) + (size_t)t0[u] * H * io_bytes(c.dtype);
+                if (fgather) {  // fp8: each token's row quantised once; bf16: nothing to move
+                    if (c.dtype == MOE_FP8_E4M3)
+                        ce = launch_quantize_rows(c, Tu, xu, xq, xq_scale, Tu, comm_grid, q);
+                    break;
+                }
+                if (!fused && plan_dispatch_fusable(c, Tu)) break;  // done with the plan
                 ce = launch_dispatch(c, Tu, xu, slot_of, xe, xe_scale, L.rows, comm_grid, q);
                 break;
             }
             case MOE_OP_FFN: {
                 FfnArgs fa{counts, offsets, L.rows, xe, xe_scale, a->w13, a->w13_scale, a->w2, a->w2_scale,
                            ye, b + L.ffn, err, two && u == 1 ? 1 : 0, L.rows, (int64_t)Tu * (c.top_k + c.num_shared)};
+                if (fused) {
+                    fa.token_of = token_of;
+                    fa.gT = Tu;
+                }
+                if (fgather) {
+                    fa.gx = c.dtype == MOE_FP8_E4M3 ? static_cast<const void*>(xq) : static_cast<const void*>(xu);
+                    fa.gx_scale = c.dtype == MOE_FP8_E4M3 ? xq_scale : nullptr;
+                }
+                if (fcombine) {
+                    fa.slot_of = slot_of;
+                    fa.topk_w = w_u;
+                    fa.y = static_cast<char*>(a->y) + (size_t)t0[u] * H * io_bytes(c.dtype);
+                    fa.cnt = reinterpret_cast<int32_t*>(b + L.comb_cnt);
+                    // shared experts first: a token's shared row is then never the last of
+                    // its rows, and the slabs completed per tile stay few
+                    fa.reverse = 1;
+                }
                 ce = launch_ffn(c, fa, ffn_grid, q);
                 break;
             }

@@ -46,6 +46,37 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_fp8_kernel(
     }
 }
 
+// Fused gather (fp8 layers): every token's row quantised once -- e4m3 codes x_q [T][H]
+// and the power-of-two 1x128 scales, column-major (group g of token t at g * scale_cs +
+// t) -- with the arithmetic of dispatch_fp8_kernel, so the expert FFN that gathers x_q
+// rows by token sees the bytes dispatch would have written to each slot.
+__global__ void __launch_bounds__(kDispatchThreads) quantize_rows_kernel(int T, int H, const uint4* __restrict__ x,
+                                                                         uint2* __restrict__ xq,
+                                                                         float* __restrict__ xs, int64_t scale_cs) {
+    pdl_begin();
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int nvec = H / 8;
+    const int nslices = (nvec + 127) / 128;
+    const int items = T * nslices;
+    for (int it = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items; it += nwarps) {
+        const int t = it / nslices;
+        const int vbeg = (it - t * nslices) * 128;
+        dispatch_fp8_item(1, nvec, x + (size_t)t * nvec, vbeg, min(nvec, vbeg + 128), lane == 0 ? t : -1, xq, xs,
+                          scale_cs, lane);
+    }
+}
+
+cudaError_t launch_quantize_rows(const moe_config& c, int T, const void* x, void* xq, float* xs, int64_t scale_cs,
+                                 int grid_cap, cudaStream_t st) {
+    if (T <= 0) return cudaSuccess;
+    const long items = (long)T * ((c.hidden / 8 + 127) / 128);
+    int grid = (int)((items + 7) / 8);
+    if (grid > grid_cap) grid = grid_cap;
+    return launch_pdl(quantize_rows_kernel, grid, kDispatchThreads, 0, st, T, c.hidden, static_cast<const uint4*>(x),
+                      static_cast<uint2*>(xq), xs, scale_cs);
+}
+
 cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int32_t* slot_of,
                             void* xe, float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st) {
     if (T <= 0) return cudaSuccess;

@@ -33,7 +33,10 @@ static int64_t rows_estimate(const moe_config& c, const FfnArgs& a) {
     return a.max_rows > pad ? a.max_rows - pad : 0;
 }
 
+bool ffn_tc_selected(const moe_config& c) { return !force_simt() && ffn_tc_supported(c); }
+
 cudaError_t launch_ffn(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st) {
+    if (a.token_of) return launch_ffn_tc(c, a, grid_cap, st);  // fused gather / combine: one-CTA kernels
     if (!force_simt() && ffn_tc_supported(c)) {
         // prefill-sized batches: 256 x 256 tiles on CTA pairs; decode: one CTA per tile
         if (ffn_pair_preferred(c, rows_estimate(c, a))) return launch_ffn_pair(c, a, grid_cap, st);

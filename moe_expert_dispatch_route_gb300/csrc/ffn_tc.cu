@@ -103,6 +103,22 @@ struct TcParams {
     int dense_rows;        // counts == nullptr: one dense matrix of this many rows
     const void* resid;     // bf16 down: added to the product before rounding ([rows][H])
     int64_t inject_ns;     // test hook: > 0 = the producer's first wait runs out after this long
+    // Fused gather (up kernels): A row r is row gather[r] (its token) of tmG -- x, or x_q
+    // for fp8, with a box one row high -- fetched with tile::gather4; null: A rows are
+    // rows of the dispatched xe (tmA).  zero / zero_n: the combine counters, cleared here.
+    const int32_t* gather;
+    CUtensorMap tmG;
+    int32_t* zero;
+    int64_t zero_n;
+    // Fused combine (down kernels): see combine_slab.  comb_token: token of each row;
+    // comb_slot / comb_w: slot_of [T][kk] / topk_w [T][k]; comb_y: y [T][H]; comb_cnt:
+    // per (token, slab of comb_cols columns) arrival counters, zero at launch.
+    const int32_t* comb_token;
+    const int32_t* comb_slot;
+    const float* comb_w;
+    void* comb_y;
+    int32_t* comb_cnt;
+    int comb_k, comb_kk, comb_cols;
 };
 
 struct Smem {
@@ -272,6 +288,142 @@ __device__ void producer(const TcParams& p, const Smem& s, int total) {
     }
 }
 
+// Clears the fused combine's counters (up kernel; the down kernel reads them only after
+// its dependency wait, i.e. after this whole grid has finished).
+__device__ __forceinline__ void zero_counters(const TcParams& p) {
+    if (!p.zero) return;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p.zero_n; i += (int64_t)gridDim.x * blockDim.x)
+        p.zero[i] = 0;
+}
+
+// Fused gather (up kernels of both types: 48 KB stages of A 16 KB + B 32 KB), whole
+// warp: lane 0 waits for the stage, announces its bytes and loads B; lane i gathers A
+// rows 4i .. 4i+3 of the tile -- the rows of x (or x_q) of their tokens -- with one
+// tile::gather4 copy into 512 bytes of the stage at 512 i.  Rows past the tile's count
+// read token 0 (their results are never stored).
+template <int kKElems>
+__device__ void producer_gather(const TcParams& p, const Smem& s, int total) {
+    const int lane = threadIdx.x & 31;
+    int inj = lane == 0 ? (int)injected_failure(p, s) : 0;
+    if (__shfl_sync(0xffffffffu, inj, 0)) return;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t pending = 0, pend_par = 0;  // lane 0: per stage, a load in flight and its parity
+    bool ok = true;
+    for (int lin = blockIdx.x; lin < total && ok; lin += gridDim.x) {
+        const Tile t = decode_tile(p, s, total, lin);
+        int tok[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * lane + i;
+            const int v = r < t.rows ? __ldg(p.gather + t.row0 + r) : 0;
+            tok[i] = v < 0 ? 0 : v;
+        }
+        const int ngather = (t.rows + 3) >> 2;
+        const uint32_t tx = (uint32_t)(ngather * 512 + kBBytes);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            int good = 1;
+            if (lane == 0) good = tc::mbar_wait(&s.empty[stage], phase ^ 1u, s.abort);
+            if (!__shfl_sync(0xffffffffu, good, 0)) {
+                ok = false;
+                break;
+            }
+            uint8_t* a = s.stages + (size_t)stage * kStageBytes;
+            if (lane == 0) {
+                tc::mbar_arrive_expect_tx(&s.full[stage], tx);
+                tc::tma_load_3d(a + kABytes, &p.tmB, &s.full[stage], kb * kKElems, t.nt * 128, 2 * t.e);
+                pending |= 1u << stage;
+                pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+            }
+            __syncwarp();
+            if (lane < ngather)
+                tc::tma_gather4(a + 512 * lane, &p.tmG, &s.full[stage], kb * kKElems, tok[0], tok[1], tok[2], tok[3]);
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        fail(s, p.err);
+        for (int st = 0; st < kStages; ++st)  // every lane's copies complete on full[st]
+            if ((pending >> st) & 1u) {
+                const uint64_t t0 = tc::globaltimer();
+                while (!tc::mbar_try_wait(&s.full[st], (pend_par >> st) & 1u) &&
+                       tc::globaltimer() - t0 < tc::kWaitTimeoutNs) {
+                }
+            }
+    }
+}
+
+// Fused combine, whole warp, after this thread's row has stored slab `slab` (p.comb_cols
+// columns, the same for the warp) of its ye row: the row is counted for its token, and
+// the last of the token's k+S rows to store the slab forms that slab of y[token] exactly
+// as moe_combine does -- sum over j in order of w_j * ye[slot_of[token][j]] (weight 1
+// for the shared experts) with fp32 fused multiply-adds, one rounding.  An entry the
+// plan did not place never arrives, so its token's slab is left unwritten (the plan has
+// raised MOE_ERR_CAPACITY / MOE_ERR_BAD_INDEX).
+__device__ __forceinline__ void combine_slab(const TcParams& p, bool valid, int64_t row, int slab) {
+    const int lane = threadIdx.x & 31;
+    const int nslab = p.H / p.comb_cols;
+    int tok = -1;
+    bool last = false;
+    if (valid) {
+        tok = __ldg(p.comb_token + row);
+        if (tok >= 0) {
+            __threadfence();  // this row's slab is visible before it is counted
+            last = atomicAdd(p.comb_cnt + (int64_t)tok * nslab + slab, 1) == p.comb_kk - 1;
+        }
+    }
+    uint32_t m = __ballot_sync(0xffffffffu, last);
+    if (!m) return;
+    __threadfence();  // the other rows' slabs, counted before, are visible to the warp
+    __syncwarp();
+    const int kk = p.comb_kk, k = p.comb_k;
+    const int nv = p.comb_cols / 8;  // 16-byte vectors of the slab (8 bf16 each)
+    const int64_t hv = p.H / 8;
+    const uint4* ye = static_cast<const uint4*>(p.out);
+    while (m) {
+        const int l = __ffs(m) - 1;
+        m &= m - 1;
+        const int t = __shfl_sync(0xffffffffu, tok, l);
+        const int my_slot = lane < kk ? __ldg(p.comb_slot + (int64_t)t * kk + lane) : -1;
+        const float my_w = lane < k ? __ldg(p.comb_w + (int64_t)t * k + lane) : 1.0f;
+        const int64_t v = (int64_t)slab * nv + lane;
+        const bool act = lane < nv;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int j0 = 0; j0 < kk; j0 += 8) {
+            uint4 val[8];
+            int r[8];
+            float wj[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u;
+                r[u] = __shfl_sync(0xffffffffu, my_slot, j & 31);
+                wj[u] = __shfl_sync(0xffffffffu, my_w, j & 31);
+                if (j >= kk) r[u] = -1;
+                if (r[u] >= 0 && act) val[u] = __ldcg(ye + (int64_t)r[u] * hv + v);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (r[u] < 0 || !act) continue;
+                const uint32_t wd[4] = {val[u].x, val[u].y, val[u].z, val[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(wj[u], bf16_bits_to_f((uint16_t)(wd[i] & 0xffffu)), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(wj[u], bf16_bits_to_f((uint16_t)(wd[i] >> 16)), acc[2 * i + 1]);
+                }
+            }
+        }
+        if (act)
+            static_cast<uint4*>(p.comb_y)[(int64_t)t * hv + v] =
+                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                           pack_bf16x2(acc[6], acc[7]));
+    }
+}
+
 __device__ void mma_issuer(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
     int stage = 0;
     uint32_t phase = 0;
@@ -320,7 +472,7 @@ __device__ void mma_issuer(const TcParams& p, const Smem& s, int total, uint32_t
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
-template <bool kUp>
+template <bool kUp, bool kComb>
 __device__ void epilogue(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -394,12 +546,15 @@ __device__ void epilogue(const TcParams& p, const Smem& s, int total, uint32_t t
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&s.tempty[buf]);
+        if (kComb) combine_slab(p, valid, row, t.nt);  // slabs of the tile's 256 columns
         buf ^= 1;
         if (buf == 0) acc_phase ^= 1u;
     }
 }
 
-template <bool kUp>
+// kComb (down kernels): the fused combine in the epilogue (a separate instantiation, so
+// the plain kernels keep their registers)
+template <bool kUp, bool kComb>
 __global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, kStages, kStageBytes, 0);
@@ -430,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_c
     tc::pdl_launch_dependents();
     tc::pdl_wait();
     if (warp == 2) scan_tiles(p, s);
+    zero_counters(p);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -437,11 +593,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_bf16_kernel(const __grid_c
     const int total = s.tstart[p.NE];
 
     if (warp == 0) {
-        if (lane == 0) producer<kUp, kBK>(p, s, total);
+        if (kUp && p.gather) producer_gather<kBK>(p, s, total);
+        else if (lane == 0) producer<kUp, kBK>(p, s, total);
     } else if (warp == 1) {
         if (lane == 0) mma_issuer(p, s, total, tmem_base);
     } else {
-        epilogue<kUp>(p, s, total, tmem_base);
+        epilogue<kUp, kComb>(p, s, total, tmem_base);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -541,7 +698,9 @@ __device__ __forceinline__ void cursor_tile(const TcParams& p, const Smem& s, in
     for (int i = 0; i < 4; ++i) {
         const int rr = 32 * i + lane;
         const int64_t row = (int64_t)t.row0 + rr;
-        c.arow[i] = (rr < t.rows && row < p.max_rows) ? p.a_scale + row * p.a_rs : nullptr;
+        int64_t src = -1;  // the scale row: the row itself, or its token when gathering
+        if (rr < t.rows && row < p.max_rows) src = p.gather ? (int64_t)__ldg(p.gather + row) : row;
+        c.arow[i] = src >= 0 ? p.a_scale + src * p.a_rs : nullptr;
     }
     // B rows 0-127 and 128-255 of the tile: up, the gate and the up n-block; down, two
     // consecutive 128-row blocks of W2
@@ -687,7 +846,7 @@ __device__ __forceinline__ void release_acc(const Smem& s, int buf) {
 }
 
 // Eight warps, two per TMEM lane quarter; `half` selects half of the tile's columns.
-template <bool kUp>
+template <bool kUp, bool kComb>
 __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
     using G = F8<kUp>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -766,6 +925,33 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
                 for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                 if (half == 0) p.out_scale[(int64_t)t.nt * p.max_rows + row] = scalbnf(1.0f, se);
             }
+        } else if (kComb) {
+            // fused combine: the accumulator in two passes of 64 columns (registers for the
+            // combine), released after the second
+            uint16_t* yrow = static_cast<uint16_t*>(p.out) + row * p.H + t.nt * G::N + 128 * half;
+#pragma unroll 1
+            for (int pass = 0; pass < 2; ++pass) {
+                uint32_t a[2][32];
+                if (busy) {
+                    tc::tmem_ld32(tb + 128 * half + 64 * pass, a[0]);
+                    tc::tmem_ld32(tb + 128 * half + 64 * pass + 32, a[1]);
+                    tc::tmem_wait_ld();
+                }
+                if (pass == 1) release_acc(s, buf);
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(yrow + 64 * pass);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[4 * c + i] = make_uint4(
+                                pack_bf16x2(__uint_as_float(a[c][8 * i]), __uint_as_float(a[c][8 * i + 1])),
+                                pack_bf16x2(__uint_as_float(a[c][8 * i + 2]), __uint_as_float(a[c][8 * i + 3])),
+                                pack_bf16x2(__uint_as_float(a[c][8 * i + 4]), __uint_as_float(a[c][8 * i + 5])),
+                                pack_bf16x2(__uint_as_float(a[c][8 * i + 6]), __uint_as_float(a[c][8 * i + 7])));
+                }
+            }
+            combine_slab(p, valid, row, t.nt * 2 + half);  // this warp's 128 columns
         } else {
             uint32_t a[4][32];  // columns 128*half .. +127 of the 256-wide tile
             if (busy) {
@@ -796,7 +982,7 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
     if (!ok) fail(s, p.err);
 }
 
-template <bool kUp>
+template <bool kUp, bool kComb>
 __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_constant__ TcParams p) {
     using G = F8<kUp>;
     extern __shared__ uint8_t smem_raw[];
@@ -826,6 +1012,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_
     tc::pdl_launch_dependents();
     tc::pdl_wait();  // see the bf16 kernel: nothing from upstream is read before this
     if (warp == 2) scan_tiles(p, s);
+    zero_counters(p);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -833,13 +1020,14 @@ __global__ void __launch_bounds__(kF8Threads, 1) ffn_tc_fp8_kernel(const __grid_
     const int total = s.tstart[p.NE];
 
     if (warp == 0) {
-        if (lane == 0) producer_f8<kUp>(p, s, total);
+        if (kUp && p.gather) producer_gather<kF8BK>(p, s, total);
+        else if (lane == 0) producer_f8<kUp>(p, s, total);
     } else if (warp == 1) {
         if (lane == 0) mma_issuer_f8<kUp>(p, s, total, tmem_base);
     } else if (warp < kF8FirstEpiWarp) {
         scale_stager_f8<kUp>(p, s, total, warp - 2);
     } else {
-        epilogue_f8<kUp>(p, s, total, tmem_base);
+        epilogue_f8<kUp, kComb>(p, s, total, tmem_base);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -871,9 +1059,9 @@ bool make_map_w13(CUtensorMap* m, const void* base, uint64_t K, uint64_t I, uint
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kUp, bool kFp8>
+template <bool kUp, bool kFp8, bool kComb = false>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
-    auto kern = kFp8 ? ffn_tc_fp8_kernel<kUp> : ffn_tc_bf16_kernel<kUp>;
+    auto kern = kFp8 ? ffn_tc_fp8_kernel<kUp, kComb> : ffn_tc_bf16_kernel<kUp, kComb>;
     const size_t smem = kFp8 ? kF8SmemBytes<kUp> : kSmemBytes;
     cudaError_t e = ensure_max_dynamic_smem(kern, (int)smem);
     if (e != cudaSuccess) return e;
@@ -967,7 +1155,31 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     up.b_scale = a.w13_scale;
     up.out_scale = h_scale;
     up.inject_ns = wait_injection_ns();
+    if (a.token_of && a.gx) {  // fused gather: A rows straight from x / x_q by token
+        if (!make_tma_map_2d(&up.tmG, a.gx, (uint64_t)H, (uint64_t)a.gT, fp8, 1)) return cudaErrorInvalidValue;
+        up.gather = a.token_of;
+        up.a_scale = a.gx_scale;
+        up.a_rs = 1;
+        up.a_cs = a.gT;
+    }
+    if (a.token_of && a.y) {  // the fused combine's counters start at zero
+        up.zero = a.cnt;
+        up.zero_n = (int64_t)a.gT * (H / 128);
+    }
     TcParams dn = up;
+    dn.gather = nullptr;
+    dn.zero = nullptr;
+    dn.zero_n = 0;
+    if (a.y) {  // fused combine in the down kernel's epilogue
+        dn.comb_token = a.token_of;
+        dn.comb_slot = a.slot_of;
+        dn.comb_w = a.topk_w;
+        dn.comb_y = a.y;
+        dn.comb_cnt = a.cnt;
+        dn.comb_k = c.top_k;
+        dn.comb_kk = c.top_k + c.num_shared;
+        dn.comb_cols = fp8 ? 128 : kBN;
+    }
     for (int i = 0; i < kNumABoxes; ++i)
         if (!make_map(&dn.tmA[i], h, (uint64_t)I, (uint64_t)a.max_rows, fp8, a_box_rows(i)))
             return cudaErrorInvalidValue;
@@ -985,6 +1197,8 @@ cudaError_t launch_ffn_tc(const moe_config& c, const FfnArgs& a, int grid_cap, c
     dn.out_scale = nullptr;
     cudaError_t e = fp8 ? launch_one<true, true>(up, grid, st) : launch_one<true, false>(up, grid, st);
     if (e != cudaSuccess) return e;
+    if (a.y)
+        return fp8 ? launch_one<false, true, true>(dn, grid, st) : launch_one<false, false, true>(dn, grid, st);
     return fp8 ? launch_one<false, true>(dn, grid, st) : launch_one<false, false>(dn, grid, st);
 }
 

@@ -66,6 +66,9 @@ cudaError_t launch_plan_dispatch(const moe_config& c, int T, const int32_t* ids,
 // then reads 32 consecutive rows' scales in one request).
 cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int32_t* slot_of,
                             void* xe, float* xe_scale, int64_t scale_cs, int grid_cap, cudaStream_t st);
+// fused gather, fp8: x [T][H] bf16 -> x_q [T][H] e4m3 + scales column-major [H/128][scale_cs]
+cudaError_t launch_quantize_rows(const moe_config& c, int T, const void* x, void* xq, float* xs, int64_t scale_cs,
+                                 int grid_cap, cudaStream_t st);
 cudaError_t launch_combine(const moe_config& c, int T, const void* ye, const float* w,
                            const int32_t* slot_of, void* y, int grid_cap, cudaStream_t st,
                            const void* resid = nullptr);
@@ -88,8 +91,22 @@ struct FfnArgs {
     int reverse;     // walk experts in descending order (L2 reuse across ubatches)
     int64_t xs_cs;   // layout of xe_scale: 0 = row-major, else column-major with this column stride
     int64_t rows_hint = 0;  // rows actually used (tokens x (k+S)) when known, else 0
+    // Fused gather: A rows are taken by token (token_of) from gx -- x (bf16) or x_q (fp8,
+    // scales gx_scale column-major [H/128][gT]) -- instead of xe.  Fused combine (with
+    // y): the down kernel forms y [gT][H] from ye, slot_of and topk_w; cnt: gT * H/128
+    // counters (cleared by the up kernel).  The one-CTA tensor-core kernels only.
+    const int32_t* token_of = nullptr;
+    const void* gx = nullptr;
+    const float* gx_scale = nullptr;
+    int gT = 0;
+    const int32_t* slot_of = nullptr;
+    const float* topk_w = nullptr;
+    void* y = nullptr;
+    int32_t* cnt = nullptr;
 };
 cudaError_t launch_ffn(const moe_config& c, const FfnArgs& a, int grid_cap, cudaStream_t st);
+// the layer's FFN runs on the tensor-core kernels (not forced onto the CUDA cores)
+bool ffn_tc_selected(const moe_config& c);
 
 // ffn_pair.cu: the same FFN on CTA pairs (tcgen05.mma.cta_group::2, 256 x 256 tiles),
 // chosen for bf16 batches averaging at least 128 rows per expert (MOE_FFN_TILE=pair /

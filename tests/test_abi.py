@@ -233,3 +233,19 @@ def test_stack_schedule_overlap_rule_and_prefix_variant():
         # everything joins back to the compute stream
         assert ops[-1][0] == 0 and ops[-1][1] == "wait"
     assert all(o[0] == 0 for o in B.moe_stack_schedule(2, False, True))
+
+
+def test_fused_schedule_has_no_combine_and_keeps_the_overlap():
+    s = B.moe_dbo_schedule(True, B.LAYER_FUSED)
+    ops, deps = _graph(s)
+    assert not any(o[1] == "combine" for o in ops)
+    for ub in (0, 1):
+        for name in ("route", "plan", "dispatch"):
+            assert ops[_find(ops, name, ub)][0] == 1  # comm stream
+        f = _find(ops, "ffn", ub)
+        assert ops[f][0] == 0 and _find(ops, "dispatch", ub) in _ancestors(deps, f)
+    # ubatch 1's route/plan/dispatch do not wait for ubatch 0's experts
+    assert _find(ops, "ffn", 0) not in _ancestors(deps, _find(ops, "dispatch", 1))
+    # joined back to the compute stream
+    assert ops[-1][0] == 0 and ops[-1][1] == "wait"
+    assert [B.OPS[o[1]] for o in B.moe_dbo_schedule(False, B.LAYER_FUSED)] == ["route", "plan", "dispatch", "ffn"]
