@@ -29,7 +29,7 @@ _lock = threading.Lock()
 _lib = None
 
 F32, BF16, FP8 = 0, 1, 2
-GATE_SOFTMAX, GATE_SIGMOID_GROUPED = 0, 1
+GATE_SOFTMAX, GATE_SIGMOID_GROUPED, GATE_SQRT_SOFTPLUS = 0, 1, 2
 OK, BAD_INDEX, CAPACITY = 0, 1, 2
 QG = 128
 
@@ -74,6 +74,12 @@ def lib():
             L.orc_spec_exp.restype = ctypes.c_float
             L.orc_spec_sigmoid.argtypes = [ctypes.c_float]
             L.orc_spec_sigmoid.restype = ctypes.c_float
+            L.orc_spec_log1p.argtypes = [ctypes.c_float]
+            L.orc_spec_log1p.restype = ctypes.c_float
+            L.orc_spec_sqrt_softplus.argtypes = [ctypes.c_float]
+            L.orc_spec_sqrt_softplus.restype = ctypes.c_float
+            L.orc_route_hash.argtypes = [P, i32, P, P, P, i32, P, P]
+            L.orc_route_hash.restype = None
             L.orc_route.argtypes = [P, i32, P, P, P, P]
             L.orc_route.restype = None
             L.orc_plan.argtypes = [i32, i32, i32, i32, P, i32, i32, P, P, P, P]
@@ -168,6 +174,14 @@ def spec_sigmoid(x: float) -> float:
     return lib().orc_spec_sigmoid(float(x))
 
 
+def spec_log1p(y: float) -> float:
+    return lib().orc_spec_log1p(float(y))
+
+
+def spec_sqrt_softplus(x: float) -> float:
+    return lib().orc_spec_sqrt_softplus(float(x))
+
+
 def quant_row_fp8(v):
     v = _f32(v)
     n = v.shape[-1]
@@ -186,6 +200,19 @@ def route(cfg: Config, logits, bias=None):
     bias = _f32(bias)
     c = cfg.c()
     lib().orc_route(ctypes.byref(c), T, _p(logits), _p(bias), _p(ids), _p(w))
+    return ids, w
+
+
+def route_hash(cfg: Config, logits, token_ids, table):
+    """Hash routing: the experts of token t are table[token_ids[t]] (see moe_oracle.c)."""
+    logits = _f32(logits)
+    token_ids = _i32(token_ids)
+    table = _i32(table)
+    T = logits.shape[0]
+    ids = np.zeros((T, cfg.top_k), np.int32)
+    w = np.zeros((T, cfg.top_k), np.float64)
+    c = cfg.c()
+    lib().orc_route_hash(ctypes.byref(c), T, _p(logits), _p(token_ids), _p(table), table.shape[0], _p(ids), _p(w))
     return ids, w
 
 

@@ -42,6 +42,7 @@
 
 #define ORC_GATE_SOFTMAX 0
 #define ORC_GATE_SIGMOID_GROUPED 1
+#define ORC_GATE_SQRT_SOFTPLUS 2
 
 #define ORC_OK 0
 #define ORC_BAD_INDEX 1
@@ -172,6 +173,50 @@ float orc_spec_sigmoid(float x) {
 }
 
 /* ------------------------------------------------------------------------- */
+/* reading: the specified log1p and sqrt-softplus used by the DeepSeek-V4      */
+/* shaped gate's expert SELECTION ("DeepEP HT: full decode CUDA graphs via    */
+/* worst-token dispatch", file table and commit messages, name a              */
+/* sqrt-softplus top-k op and give no formula).  The score is                 */
+/* s(x) = sqrt(softplus(x)), softplus(x) = ln(1 + e^x), written as            */
+/* max(x, 0) + log1p(e^-|x|) on x clamped to [-80, 80].  log1p(y), y in       */
+/* [0, 1], is the series 2 atanh(z) = 2 (z + z^3/3 + ... + z^15/15) of        */
+/* z = y / (2 + y) <= 1/3, in Horner form in z^2 with fused multiply-adds.     */
+/* Every operation binary32 round-to-nearest; sqrt is the correctly rounded  */
+/* IEEE square root.                                                          */
+/* ------------------------------------------------------------------------- */
+static const float SPEC_I3 = 0x1.555556p-2f;  /* 1/3 */
+static const float SPEC_I5 = 0x1.99999ap-3f;  /* 1/5 */
+static const float SPEC_I7 = 0x1.24924ap-3f;  /* 1/7 */
+static const float SPEC_I9 = 0x1.c71c72p-4f;  /* 1/9 */
+static const float SPEC_I11 = 0x1.745d18p-4f; /* 1/11 */
+static const float SPEC_I13 = 0x1.3b13b2p-4f; /* 1/13 */
+static const float SPEC_I15 = 0x1.111112p-4f; /* 1/15 */
+
+float orc_spec_log1p(float y) {
+    float z = y / (2.0f + y);
+    float z2 = z * z;
+    float p = SPEC_I15;
+    p = fmaf(p, z2, SPEC_I13);
+    p = fmaf(p, z2, SPEC_I11);
+    p = fmaf(p, z2, SPEC_I9);
+    p = fmaf(p, z2, SPEC_I7);
+    p = fmaf(p, z2, SPEC_I5);
+    p = fmaf(p, z2, SPEC_I3);
+    p = fmaf(p, z2, 1.0f);
+    return (2.0f * z) * p;
+}
+
+float orc_spec_sqrt_softplus(float x) {
+    float c = x < -80.0f ? -80.0f : (x > 80.0f ? 80.0f : x);
+    float e = orc_spec_exp(-fabsf(c));
+    float sp = fmaxf(c, 0.0f) + orc_spec_log1p(e);
+    return sqrtf(sp);
+}
+
+/* sqrt(softplus(x)) in double (the weights). */
+static double sqrt_softplus_d(double x) { return sqrt(x > 30.0 ? x + log1p(exp(-x)) : log1p(exp(x))); }
+
+/* ------------------------------------------------------------------------- */
 /* Route                                                                     */
 /* ------------------------------------------------------------------------- */
 
@@ -216,9 +261,28 @@ void orc_route_softmax(int32_t T, int32_t E, int32_t k, int32_t renorm, const fl
  * kept groups by choice score (equal -> lower id), in descending order.  Weight =
  * the plain sigmoid of the chosen logits (no bias), divided by their sum when
  * renormalising, times routed_scale. */
+/* reading (DeepSeek-V4 shaped gate): the same group-limited selection with the score
+ * s_e = the specified sqrt-softplus of l_e instead of sigma (n_group = 1: plain top-k);
+ * weight = sqrt(softplus(l)) of the chosen (no bias), divided by their sum when
+ * renormalising, times routed_scale.  sqrt_softplus = 1 selects it. */
+static void route_grouped(int32_t T, int32_t E, int32_t k, int32_t n_group, int32_t topk_group, int32_t renorm,
+                          double routed_scale, const float* logits, const float* bias, int32_t* ids, double* w,
+                          int sqrt_softplus);
+
 void orc_route_sigmoid_grouped(int32_t T, int32_t E, int32_t k, int32_t n_group,
                                int32_t topk_group, int32_t renorm, double routed_scale,
                                const float* logits, const float* bias, int32_t* ids, double* w) {
+    route_grouped(T, E, k, n_group, topk_group, renorm, routed_scale, logits, bias, ids, w, 0);
+}
+
+void orc_route_sqrt_softplus(int32_t T, int32_t E, int32_t k, int32_t n_group, int32_t topk_group, int32_t renorm,
+                             double routed_scale, const float* logits, const float* bias, int32_t* ids, double* w) {
+    route_grouped(T, E, k, n_group, topk_group, renorm, routed_scale, logits, bias, ids, w, 1);
+}
+
+static void route_grouped(int32_t T, int32_t E, int32_t k, int32_t n_group, int32_t topk_group, int32_t renorm,
+                          double routed_scale, const float* logits, const float* bias, int32_t* ids, double* w,
+                          int sqrt_softplus) {
     int32_t gsz = E / n_group;
     float* s = (float*)malloc(sizeof(float) * (size_t)E);
     float* c = (float*)malloc(sizeof(float) * (size_t)E);
@@ -228,7 +292,7 @@ void orc_route_sigmoid_grouped(int32_t T, int32_t E, int32_t k, int32_t n_group,
     for (int32_t t = 0; t < T; ++t) {
         const float* l = logits + (size_t)t * E;
         for (int32_t e = 0; e < E; ++e) {
-            s[e] = orc_spec_sigmoid(l[e]);
+            s[e] = sqrt_softplus ? orc_spec_sqrt_softplus(l[e]) : orc_spec_sigmoid(l[e]);
             c[e] = s[e] + (bias ? bias[e] : 0.0f);
         }
         for (int32_t g = 0; g < n_group; ++g) {
@@ -259,13 +323,13 @@ void orc_route_sigmoid_grouped(int32_t T, int32_t E, int32_t k, int32_t n_group,
             chosen[best] = 1;
             ids[(size_t)t * k + j] = best;
         }
-        double sum = 0.0;
-        for (int32_t j = 0; j < k; ++j)
-            sum += 1.0 / (1.0 + exp(-(double)l[ids[(size_t)t * k + j]]));
+        double sum = 0.0, sj[32];
         for (int32_t j = 0; j < k; ++j) {
-            double sj = 1.0 / (1.0 + exp(-(double)l[ids[(size_t)t * k + j]]));
-            w[(size_t)t * k + j] = (renorm ? sj / sum : sj) * routed_scale;
+            double x = (double)l[ids[(size_t)t * k + j]];
+            sj[j] = sqrt_softplus ? sqrt_softplus_d(x) : 1.0 / (1.0 + exp(-x));
+            sum += sj[j];
         }
+        for (int32_t j = 0; j < k; ++j) w[(size_t)t * k + j] = (renorm ? sj[j] / sum : sj[j]) * routed_scale;
     }
     free(s);
     free(c);
@@ -278,9 +342,38 @@ void orc_route(const orc_cfg* cfg, int32_t T, const float* logits, const float* 
                int32_t* ids, double* w) {
     if (cfg->gate == ORC_GATE_SOFTMAX)
         orc_route_softmax(T, cfg->num_experts, cfg->top_k, cfg->renormalize, logits, ids, w);
+    else if (cfg->gate == ORC_GATE_SQRT_SOFTPLUS)
+        orc_route_sqrt_softplus(T, cfg->num_experts, cfg->top_k, cfg->n_group, cfg->topk_group, cfg->renormalize,
+                                cfg->routed_scale, logits, bias, ids, w);
     else
         orc_route_sigmoid_grouped(T, cfg->num_experts, cfg->top_k, cfg->n_group, cfg->topk_group,
                                   cfg->renormalize, cfg->routed_scale, logits, bias, ids, w);
+}
+
+/* reading (hash routing of the DeepSeek-V4 shaped layers; the pages name hash-routing
+ * metadata of int32 expert ids passed to the sqrt-softplus top-k op and give no
+ * formula): token t's k experts are row token_ids[t] of a fixed table [vocab][k]; the
+ * weights are the sqrt-softplus gate's, sqrt(softplus(l)) of those experts divided by
+ * their sum when renormalising, times routed_scale.  A token id outside [0, vocab)
+ * gives ids -1 and weights 0; a table entry outside [0, E) is passed on (the plan
+ * reports it) with weight 0. */
+void orc_route_hash(const orc_cfg* cfg, int32_t T, const float* logits, const int32_t* token_ids,
+                    const int32_t* table, int32_t vocab, int32_t* ids, double* w) {
+    int32_t E = cfg->num_experts, k = cfg->top_k;
+    for (int32_t t = 0; t < T; ++t) {
+        int32_t tid = token_ids[t];
+        double sj[32], sum = 0.0;
+        for (int32_t j = 0; j < k; ++j) {
+            int32_t e = (tid >= 0 && tid < vocab) ? table[(size_t)tid * k + j] : -1;
+            ids[(size_t)t * k + j] = e;
+            sj[j] = (e >= 0 && e < E) ? sqrt_softplus_d((double)logits[(size_t)t * E + e]) : 0.0;
+            sum += sj[j];
+        }
+        for (int32_t j = 0; j < k; ++j) {
+            double v = (cfg->renormalize && sum > 0.0) ? sj[j] / sum : sj[j];
+            w[(size_t)t * k + j] = v * cfg->routed_scale;
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------- */
