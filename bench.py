@@ -765,7 +765,8 @@ def _ocfg(wl):
     import oracle
     return oracle.Config(hidden=wl.hidden, inter=wl.inter, num_experts=wl.num_experts,
                          num_shared=wl.num_shared, top_k=wl.top_k,
-                         gate=oracle.GATE_SOFTMAX if wl.gate == "softmax" else oracle.GATE_SIGMOID_GROUPED,
+                         gate={"softmax": oracle.GATE_SOFTMAX, "sigmoid_grouped": oracle.GATE_SIGMOID_GROUPED,
+                               "sqrt_softplus": oracle.GATE_SQRT_SOFTPLUS}[wl.gate],
                          renormalize=int(wl.renormalize), n_group=wl.n_group, topk_group=wl.topk_group,
                          routed_scale=wl.routed_scale,
                          dtype={"f32": oracle.F32, "bf16": oracle.BF16, "fp8": oracle.FP8}[wl.dtype])

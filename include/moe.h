@@ -71,7 +71,7 @@ typedef enum {
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype;
-typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID_GROUPED = 1 } moe_gate;
+typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID_GROUPED = 1, MOE_GATE_SQRT_SOFTPLUS = 2 } moe_gate;
 
 /* Shape of one layer.  E = num_experts routed experts, S = num_shared always-on
  * experts (stored after the routed ones: expert ids E .. E+S-1), k = top_k.
@@ -81,7 +81,7 @@ typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID_GROUPED = 1 } moe_gate;
  *   MOE_FP8_E4M3  x, ye, y bf16; xe and h e4m3 with one fp32 power-of-two scale per
  *                 1x128 group of a row; weights e4m3 with one fp32 scale per
  *                 128x128 block.  hidden and inter must be multiples of 128.
- * Limits: k >= 1, k + S <= 32, k <= E, E + S <= 512; grouped gate: E % n_group == 0,
+ * Limits: k >= 1, k + S <= 32, k <= E, E + S <= 512; grouped gates: E % n_group == 0,
  * 2 <= E / n_group, n_group <= 32, 1 <= topk_group <= n_group,
  * k <= topk_group * (E / n_group). */
 typedef struct {
@@ -92,9 +92,9 @@ typedef struct {
     int32_t top_k;        /* k */
     int32_t gate;         /* moe_gate */
     int32_t renormalize;  /* 1: chosen weights sum to 1 (times routed_scale) */
-    int32_t n_group;      /* grouped gate only */
-    int32_t topk_group;   /* grouped gate only */
-    float routed_scale;   /* grouped gate only: multiplies the routed weights */
+    int32_t n_group;      /* grouped gates only */
+    int32_t topk_group;   /* grouped gates only */
+    float routed_scale;   /* grouped gates only: multiplies the routed weights */
     int32_t dtype;        /* moe_dtype */
 } moe_config;
 
@@ -112,6 +112,12 @@ typedef struct {
  *     (equal -> lower group id); the k best c inside them are chosen (equal -> lower
  *     id); w = sigmoid(l) of the chosen (no bias), / their sum if renormalize, times
  *     routed_scale.  Selection is bit-reproducible; weights are fp32.
+ *   sqrt-softplus gate (DeepSeek-V4 shaped; the pages name a sqrt-softplus top-k op
+ *     and give no formula -- reading): the grouped gate with the score
+ *     s_e = sqrt(softplus(l_e)), softplus specified as max(x, 0) + log1p(e^-|x|) on
+ *     [-80, 80] with the library's specified exp and a specified log1p (the 2 atanh
+ *     series to z^15), then IEEE sqrt; n_group = 1 is plain top-k; w = sqrt(softplus(l))
+ *     of the chosen, / their sum if renormalize, times routed_scale.
  * logits   device fp32 [T][E], row-major.  The gates are defined for finite logits;
  *          a NaN logit (or score) is ranked as -inf, so every id written is in [0, E)
  *          whatever the input holds (the weights of such a row are unspecified).
@@ -121,6 +127,23 @@ typedef struct {
  * T = 0 is a no-op. */
 MOE_API moe_status moe_route(const moe_config* cfg, int32_t T, const float* logits, const float* bias,
                      int32_t* topk_ids, float* topk_w, int32_t max_ctas, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_route_hash -- hash routing of the DeepSeek-V4-shaped layers (the pages name
+ * hash-routing metadata, int32 expert ids, passed to the sqrt-softplus top-k op;
+ * reading): token t's k experts are row token_ids[t] of a fixed table, and the weights
+ * are the sqrt-softplus gate's -- sqrt(softplus(l)) of those experts, / their sum if
+ * renormalize, times routed_scale.  Requires cfg->gate == MOE_GATE_SQRT_SOFTPLUS
+ * (else MOE_ERR_UNSUPPORTED).
+ * logits    device fp32 [T][E];  token_ids device int32 [T];
+ * table     device int32 [vocab][k];
+ * topk_ids  device int32 [T][k] (out): the table's entries, passed on unchecked (an
+ *           entry outside [0, E) gets weight 0, and moe_plan flags it); a token id
+ *           outside [0, vocab) gives ids -1 and weights 0 for its row.
+ * topk_w    device fp32 [T][k] (out). */
+MOE_API moe_status moe_route_hash(const moe_config* cfg, int32_t T, const float* logits, const int32_t* token_ids,
+                                  const int32_t* table, int32_t vocab, int32_t* topk_ids, float* topk_w,
+                                  int32_t max_ctas, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_plan -- per-expert counts, aligned exclusive prefix sums and the row ("slot")

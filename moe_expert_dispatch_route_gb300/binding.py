@@ -16,7 +16,7 @@ import torch
 from . import build as _build
 
 F32, BF16, FP8_E4M3 = 0, 1, 2
-GATE_SOFTMAX, GATE_SIGMOID_GROUPED = 0, 1
+GATE_SOFTMAX, GATE_SIGMOID_GROUPED, GATE_SQRT_SOFTPLUS = 0, 1, 2
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
           4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_CAPACITY", 7: "MOE_ERR_BAD_INDEX",
           8: "MOE_ERR_TIMEOUT"}
@@ -62,8 +62,8 @@ def config(hidden, inter, num_experts, num_shared, top_k, gate=GATE_SOFTMAX, ren
 
 def config_of(wl) -> MoeConfig:
     """MoeConfig of a workloads.Workload."""
-    return config(wl.hidden, wl.inter, wl.num_experts, wl.num_shared, wl.top_k,
-                  GATE_SOFTMAX if wl.gate == "softmax" else GATE_SIGMOID_GROUPED,
+    gate = {"softmax": GATE_SOFTMAX, "sigmoid_grouped": GATE_SIGMOID_GROUPED, "sqrt_softplus": GATE_SQRT_SOFTPLUS}
+    return config(wl.hidden, wl.inter, wl.num_experts, wl.num_shared, wl.top_k, gate[wl.gate],
                   int(wl.renormalize), wl.n_group, wl.topk_group, wl.routed_scale,
                   {"f32": F32, "bf16": BF16, "fp8": FP8_E4M3}[wl.dtype])
 
@@ -72,6 +72,7 @@ _P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_
 _CFG = ctypes.POINTER(MoeConfig)
 _SIGS = {
     "moe_route": (_I32, [_CFG, _I32, _P, _P, _P, _P, _I32, _P]),
+    "moe_route_hash": (_I32, [_CFG, _I32, _P, _P, _P, _I32, _P, _P, _I32, _P]),
     "moe_plan_rows": (_SZ, [_CFG, _I32, _I32, _I32]),
     "moe_plan_workspace_size": (_SZ, [_CFG, _I32]),
     "moe_plan": (_I32, [_CFG, _I32, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _I32, _P]),
@@ -145,6 +146,12 @@ def _check(st: int, where: str):
 def moe_route(cfg, T, logits, bias, topk_ids, topk_w, max_ctas=0, stream=None):
     _check(lib().moe_route(ctypes.byref(cfg), T, _ptr(logits), _ptr(bias), _ptr(topk_ids), _ptr(topk_w),
                            max_ctas, _stream(stream)), "moe_route")
+
+
+def moe_route_hash(cfg, T, logits, token_ids, table, topk_ids, topk_w, max_ctas=0, stream=None):
+    vocab = table.shape[0] if table is not None else 0
+    _check(lib().moe_route_hash(ctypes.byref(cfg), T, _ptr(logits), _ptr(token_ids), _ptr(table), vocab,
+                                _ptr(topk_ids), _ptr(topk_w), max_ctas, _stream(stream)), "moe_route_hash")
 
 
 def moe_plan_rows(cfg, T, capacity=0, align=1) -> int:

@@ -117,7 +117,7 @@ moe_status check_config(const moe_config* c) {
     if (c->hidden <= 0 || c->inter <= 0 || E <= 0 || S < 0 || k <= 0) return MOE_ERR_INVALID_ARG;
     if (k > E || k > 32 || k + S > kMaxSlotsPerToken || E + S > kMaxExperts) return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_F32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
-    if (c->gate == MOE_GATE_SIGMOID_GROUPED) {
+    if (c->gate == MOE_GATE_SIGMOID_GROUPED || c->gate == MOE_GATE_SQRT_SOFTPLUS) {
         const int G = c->n_group, TG = c->topk_group;
         if (G <= 0 || G > 32 || E % G != 0 || E / G < 2 || TG <= 0 || TG > G || k > TG * (E / G))
             return MOE_ERR_INVALID_ARG;
@@ -168,6 +168,19 @@ moe_status moe_route(const moe_config* cfg, int32_t T, const float* logits, cons
     if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_route(*cfg, T, logits, bias, topk_ids, topk_w, grid_cap_of(max_ctas),
                                     (cudaStream_t)stream));
+}
+
+moe_status moe_route_hash(const moe_config* cfg, int32_t T, const float* logits, const int32_t* token_ids,
+                          const int32_t* table, int32_t vocab, int32_t* topk_ids, float* topk_w, int32_t max_ctas,
+                          moe_stream_t stream) {
+    moe_status s = check_config(cfg);
+    if (s != MOE_OK) return s;
+    if (cfg->gate != MOE_GATE_SQRT_SOFTPLUS) return MOE_ERR_UNSUPPORTED;
+    if (T < 0 || vocab < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!logits || !token_ids || !topk_ids || !topk_w || (vocab > 0 && !table)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_route_hash(*cfg, T, logits, token_ids, table, vocab, topk_ids, topk_w,
+                                         grid_cap_of(max_ctas), (cudaStream_t)stream));
 }
 
 size_t moe_plan_rows(const moe_config* cfg, int32_t T, int32_t capacity, int32_t align) {

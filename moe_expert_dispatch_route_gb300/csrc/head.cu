@@ -134,8 +134,10 @@ struct HeadArgs {
     int nvec;
 };
 
-template <int NPER, bool kGrouped, bool kFp8>
+// kGate: the gate (moe_gate): softmax, group-limited sigmoid or sqrt-softplus.
+template <int NPER, int kGate, bool kFp8>
 __global__ void __launch_bounds__(kPlanThreads) route_plan_dispatch_kernel(const __grid_constant__ HeadArgs a) {
+    constexpr bool kGrouped = kGate != MOE_GATE_SOFTMAX;
     extern __shared__ int head_sm[];
     pdl_begin();
     const int T = a.T, k = a.k, kk = a.k + a.S, n = T * kk;
@@ -150,8 +152,9 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_dispatch_kernel(const
         int id;
         float wt;
         if (kGrouped)
-            route_token_grouped<NPER>(t, a.E, k, a.n_group, a.topk_group, a.renorm, a.scale, a.logits, a.bias,
-                                      cs + warp * a.E, id, wt);
+            route_token_grouped<NPER, kGate == MOE_GATE_SQRT_SOFTPLUS>(t, a.E, k, a.n_group, a.topk_group, a.renorm,
+                                                                       a.scale, a.logits, a.bias, cs + warp * a.E, id,
+                                                                       wt);
         else
             route_token_softmax<NPER>(t, a.E, k, a.renorm, a.logits, id, wt);
         if (lane < k) {
@@ -199,9 +202,10 @@ bool head_fusable(const moe_config& c, int T) {
     return !head_separate() && plan_dispatch_fusable(c, T) && T <= kHeadClusterMax * kPlanWarps * kHeadTokensPerWarp;
 }
 
-template <int NPER, bool kGrouped, bool kFp8>
+template <int NPER, int kGate, bool kFp8>
 static cudaError_t launch_head_t(const HeadArgs& a, int E, int grid_cap, cudaStream_t st) {
-    auto kern = route_plan_dispatch_kernel<NPER, kGrouped, kFp8>;
+    constexpr bool kGrouped = kGate != MOE_GATE_SOFTMAX;
+    auto kern = route_plan_dispatch_kernel<NPER, kGate, kFp8>;
     const int kk = a.k + a.S;
     const size_t smem = (size_t)a.T * a.k * 4 + 2 * (size_t)a.T * kk * 4 + (kGrouped ? (size_t)kPlanWarps * E * 4 : 0);
     cudaError_t e = ensure_max_dynamic_smem(
@@ -231,13 +235,13 @@ static cudaError_t launch_head_t(const HeadArgs& a, int E, int grid_cap, cudaStr
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <bool kGrouped, bool kFp8>
+template <int kGate, bool kFp8>
 static cudaError_t launch_head_g(const HeadArgs& a, int E, int grid_cap, cudaStream_t st) {
-    if (E <= 32) return launch_head_t<1, kGrouped, kFp8>(a, E, grid_cap, st);
-    if (E <= 64) return launch_head_t<2, kGrouped, kFp8>(a, E, grid_cap, st);
-    if (E <= 128) return launch_head_t<4, kGrouped, kFp8>(a, E, grid_cap, st);
-    if (E <= 256) return launch_head_t<8, kGrouped, kFp8>(a, E, grid_cap, st);
-    return launch_head_t<16, kGrouped, kFp8>(a, E, grid_cap, st);
+    if (E <= 32) return launch_head_t<1, kGate, kFp8>(a, E, grid_cap, st);
+    if (E <= 64) return launch_head_t<2, kGate, kFp8>(a, E, grid_cap, st);
+    if (E <= 128) return launch_head_t<4, kGate, kFp8>(a, E, grid_cap, st);
+    if (E <= 256) return launch_head_t<8, kGate, kFp8>(a, E, grid_cap, st);
+    return launch_head_t<16, kGate, kFp8>(a, E, grid_cap, st);
 }
 
 cudaError_t launch_route_plan_dispatch(const moe_config& c, int T, const float* logits, const float* bias,
@@ -269,9 +273,14 @@ cudaError_t launch_route_plan_dispatch(const moe_config& c, int T, const float* 
     a.xe_scale = xe_scale;
     a.scale_cs = scale_cs;
     a.nvec = fp8 ? c.hidden / 8 : c.hidden * elt_bytes(c.dtype) / 16;
-    const bool grouped = c.gate == MOE_GATE_SIGMOID_GROUPED;
-    if (grouped) return fp8 ? launch_head_g<true, true>(a, a.E, grid_cap, st) : launch_head_g<true, false>(a, a.E, grid_cap, st);
-    return fp8 ? launch_head_g<false, true>(a, a.E, grid_cap, st) : launch_head_g<false, false>(a, a.E, grid_cap, st);
+    if (c.gate == MOE_GATE_SIGMOID_GROUPED)
+        return fp8 ? launch_head_g<MOE_GATE_SIGMOID_GROUPED, true>(a, a.E, grid_cap, st)
+                   : launch_head_g<MOE_GATE_SIGMOID_GROUPED, false>(a, a.E, grid_cap, st);
+    if (c.gate == MOE_GATE_SQRT_SOFTPLUS)
+        return fp8 ? launch_head_g<MOE_GATE_SQRT_SOFTPLUS, true>(a, a.E, grid_cap, st)
+                   : launch_head_g<MOE_GATE_SQRT_SOFTPLUS, false>(a, a.E, grid_cap, st);
+    return fp8 ? launch_head_g<MOE_GATE_SOFTMAX, true>(a, a.E, grid_cap, st)
+               : launch_head_g<MOE_GATE_SOFTMAX, false>(a, a.E, grid_cap, st);
 }
 
 }  // namespace moe

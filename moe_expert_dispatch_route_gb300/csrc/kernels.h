@@ -41,6 +41,9 @@ cudaError_t ensure_max_dynamic_smem(void (*kern)(A...), int bytes) {
 cudaError_t launch_route(const moe_config& c, int T, const float* logits, const float* bias,
                          int32_t* ids, float* w, int grid_cap, cudaStream_t st);
 
+cudaError_t launch_route_hash(const moe_config& c, int T, const float* logits, const int32_t* token_ids,
+                              const int32_t* table, int vocab, int32_t* ids, float* w, int grid_cap, cudaStream_t st);
+
 // plan.cu
 int plan_tokens_per_chunk(const moe_config& c, int T);
 int plan_num_chunks(const moe_config& c, int T);

@@ -39,6 +39,36 @@ __device__ __forceinline__ float spec_sigmoid(float x) {
     return __fdiv_rn(1.0f, __fadd_rn(1.0f, spec_exp(-c)));
 }
 
+// The DeepSeek-V4-shaped gate's score s(x) = sqrt(softplus(x)) is SPECIFIED the same
+// way: softplus(x) = max(x, 0) + log1p(e^-|x|) on x clamped to [-80, 80], e^x as above,
+// log1p(y) (y in [0, 1]) as the series 2 atanh(z) = 2 (z + z^3/3 + ... + z^15/15) of
+// z = y / (2 + y), Horner in z^2 with fused multiply-adds, each coefficient 1/n
+// rounded to binary32; then the correctly rounded square root.
+__device__ __forceinline__ float spec_log1p(float y) {
+    const float z = __fdiv_rn(y, __fadd_rn(2.0f, y));
+    const float z2 = __fmul_rn(z, z);
+    float p = 0x1.111112p-4f;             // 1/15
+    p = __fmaf_rn(p, z2, 0x1.3b13b2p-4f);  // 1/13
+    p = __fmaf_rn(p, z2, 0x1.745d18p-4f);  // 1/11
+    p = __fmaf_rn(p, z2, 0x1.c71c72p-4f);  // 1/9
+    p = __fmaf_rn(p, z2, 0x1.24924ap-3f);  // 1/7
+    p = __fmaf_rn(p, z2, 0x1.99999ap-3f);  // 1/5
+    p = __fmaf_rn(p, z2, 0x1.555556p-2f);  // 1/3
+    p = __fmaf_rn(p, z2, 1.0f);
+    return __fmul_rn(__fmul_rn(2.0f, z), p);
+}
+
+__device__ __forceinline__ float spec_sqrt_softplus(float x) {
+    const float c = x < -80.0f ? -80.0f : (x > 80.0f ? 80.0f : x);
+    const float e = spec_exp(-fabsf(c));
+    return __fsqrt_rn(__fadd_rn(fmaxf(c, 0.0f), spec_log1p(e)));
+}
+
+// sqrt(softplus(x)) for the weights (ordinary math, compared with a tolerance).
+__device__ __forceinline__ float sqrt_softplus(float x) {
+    return sqrtf(x > 30.0f ? x + log1pf(expf(-x)) : log1pf(expf(x)));
+}
+
 // A NaN score takes part in the selection as -inf: every comparison with NaN is false,
 // so without this a row of NaNs would select no expert at all.  Finite scores, the
 // only ones the gates are defined for, are unchanged.
@@ -110,9 +140,11 @@ __device__ __forceinline__ void route_token_softmax(int t, int E, int k, int ren
     out_w = my_p / z;
 }
 
-// One warp: token t of the grouped sigmoid gate.  cs: this warp's E floats of shared
-// memory.  Lane j < k returns the j-th choice and its weight.
-template <int NPER>
+// One warp: token t of the group-limited gate with the score sigma (kSqrtSoftplus =
+// false, the DeepSeek-V3 shape) or sqrt(softplus) (true, the DeepSeek-V4 shape).  cs:
+// this warp's E floats of shared memory.  Lane j < k returns the j-th choice and its
+// weight.
+template <int NPER, bool kSqrtSoftplus = false>
 __device__ __forceinline__ void route_token_grouped(int t, int E, int k, int n_group, int topk_group, int renorm,
                                                     float scale, const float* __restrict__ logits,
                                                     const float* __restrict__ bias, float* cs, int& out_id,
@@ -125,7 +157,8 @@ __device__ __forceinline__ void route_token_grouped(int t, int E, int k, int n_g
     for (int i = 0; i < NPER; ++i) {
         int e = lane + 32 * i;
         if (e < E) {
-            float s = spec_sigmoid(__ldg(l + e));
+            const float x = __ldg(l + e);
+            const float s = kSqrtSoftplus ? spec_sqrt_softplus(x) : spec_sigmoid(x);
             c[i] = nan_to_neg_inf(__fadd_rn(s, bias ? __ldg(bias + e) : 0.0f));
             cs[e] = c[i];
         } else {
@@ -184,7 +217,10 @@ __device__ __forceinline__ void route_token_grouped(int t, int E, int k, int n_g
         if (lane == j) my_id = bi;
     }
     float sj = 0.0f;
-    if (lane < k) sj = 1.0f / (1.0f + expf(-__ldg(l + (my_id < E ? my_id : 0))));
+    if (lane < k) {
+        const float x = __ldg(l + (my_id < E ? my_id : 0));
+        sj = kSqrtSoftplus ? sqrt_softplus(x) : 1.0f / (1.0f + expf(-x));
+    }
     float sum = warp_sum(sj);
     out_id = my_id;
     out_w = (renorm ? sj / sum : sj) * scale;

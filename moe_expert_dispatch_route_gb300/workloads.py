@@ -39,7 +39,7 @@ class Workload:
     num_experts: int
     num_shared: int
     top_k: int
-    gate: str = "softmax"          # "softmax" | "sigmoid_grouped"
+    gate: str = "softmax"          # "softmax" | "sigmoid_grouped" | "sqrt_softplus"
     renormalize: bool = True
     n_group: int = 1
     topk_group: int = 1

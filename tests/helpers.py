@@ -18,7 +18,8 @@ TOL = {"bf16": dict(max_abs=2e-2, rel_l2=1e-2), "fp8": dict(max_abs=None, rel_l2
 def ocfg(wl: workloads.Workload) -> oracle.Config:
     return oracle.Config(hidden=wl.hidden, inter=wl.inter, num_experts=wl.num_experts,
                          num_shared=wl.num_shared, top_k=wl.top_k,
-                         gate=oracle.GATE_SOFTMAX if wl.gate == "softmax" else oracle.GATE_SIGMOID_GROUPED,
+                         gate={"softmax": oracle.GATE_SOFTMAX, "sigmoid_grouped": oracle.GATE_SIGMOID_GROUPED,
+                               "sqrt_softplus": oracle.GATE_SQRT_SOFTPLUS}[wl.gate],
                          renormalize=int(wl.renormalize), n_group=wl.n_group, topk_group=wl.topk_group,
                          routed_scale=wl.routed_scale,
                          dtype={"f32": oracle.F32, "bf16": oracle.BF16, "fp8": oracle.FP8}[wl.dtype])
