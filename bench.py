@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--workload", default=None, choices=sorted(W.ALL),
                     help=f"default: {DEFAULT_WORKLOAD[0]} at T={DEFAULT_WORKLOAD[1]}")
     ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--experts", type=int, default=None, help="routed experts (a scaled-down shape for profiling)")
     ap.add_argument("--min-seconds", type=float, default=3.0,
                     help="repeat blocks of --steps timed steps until this much timed work has passed")
     ap.add_argument("--routing", default=None, choices=[None, "uniform", "zipf"])
@@ -83,6 +84,8 @@ def workload(args):
         wl = W.ALL[args.workload]
     if args.T:
         wl = wl.with_(T=args.T)
+    if args.experts:
+        wl = wl.with_(num_experts=args.experts)
     if args.routing:
         wl = wl.with_(routing=args.routing)
     if args.capacity is not None:
@@ -245,10 +248,10 @@ def ffn_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_tag: str, wl_name: str):
-    """DRAM bytes per launch recorded from an ncu capture in profiles/, only if the
-    FFN sources are unchanged since the capture."""
-    p = os.path.join(ROOT, "profiles", f"{kernel_tag}_{wl_name}.txt")
+def profiled_traffic(kernel_tag: str, wl):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/ (for this workload
+    and batch size), only if the FFN sources are unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", f"{kernel_tag}_{wl.name}_T{wl.T}.txt")
     if not os.path.exists(p):
         return None
     vals = {}
@@ -633,7 +636,7 @@ def ffn_roofline(B, wl, cfg, inp, dev, args, comm_sms, compute):
         achieved, peak, unit = bytes_alg / t / 1e9, pk["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = flops_alg / t / 1e12, tf / 1e12, "TFLOP/s"
-    traffic = profiled_traffic("ffn", wl.name)
+    traffic = profiled_traffic("ffn", wl) if wl.num_experts == W.ALL[wl.name].num_experts else None
 
     # the comm-side kernels of the same ubatch, each timed alone on the whole GPU, one
     # call at a time between CUDA events with L2 flushed before each call (their
