@@ -395,9 +395,19 @@ MOE_API const char* moe_status_string(moe_status s);
  * wait, limited to timeout_ns, on a barrier that nothing ever completes, before it
  * issues any copy: the wait runs out, the kernel stores MOE_ERR_TIMEOUT in err_flag,
  * skips its work, frees its tensor memory and returns normally, so the context stays
- * usable.  enable = 0 (the default) turns it off.  Process-wide, host-side only;
+ * usable.  The staged combine kernel takes the same path (its error goes to the
+ * layer's err_flag, or, called on its own, to the word moe_comm_error reads).
+ * enable = 0 (the default) turns it off.  Process-wide, host-side only;
  * enable != 0 with timeout_ns <= 0 is MOE_ERR_INVALID_ARG. */
 MOE_API moe_status moe_debug_inject_wait(int32_t enable, int64_t timeout_ns);
+
+/* ---------------------------------------------------------------------------
+ * moe_comm_error -- the library's sticky error word for moe_combine, whose signature
+ * carries no error flag: MOE_ERR_TIMEOUT once a bounded wait of its staged kernel ran
+ * out on the current device (never on a healthy GPU; see moe_debug_inject_wait), else
+ * 0.  (moe_dispatch has no waits.)  Synchronises the current device, writes the word to
+ * *code (host), and resets it to 0 when clear != 0.  code NULL: MOE_ERR_INVALID_ARG. */
+MOE_API moe_status moe_comm_error(int32_t* code, int32_t clear);
 
 #ifdef __cplusplus
 }

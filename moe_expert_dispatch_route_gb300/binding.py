@@ -96,6 +96,7 @@ _SIGS = {
     "moe_stack_schedule": (_I32, [_I32, _I32, _I32, _P, _I32]),
     "moe_status_string": (ctypes.c_char_p, [_I32]),
     "moe_debug_inject_wait": (_I32, [_I32, _I64]),
+    "moe_comm_error": (_I32, [_P, _I32]),
 }
 EXPORTS = tuple(_SIGS)
 
@@ -244,8 +245,16 @@ def moe_dbo_schedule(two_ubatches: bool, flags: int = 0):
 
 
 def moe_debug_inject_wait(enable: bool, timeout_ns: int = 0):
-    """Test hook: FFN kernels launched while enabled let a bounded wait run out (see moe.h)."""
+    """Test hook: FFN and combine kernels launched while enabled let a bounded wait run
+    out (see moe.h)."""
     _check(lib().moe_debug_inject_wait(int(enable), int(timeout_ns)), "moe_debug_inject_wait")
+
+
+def moe_comm_error(clear: bool = False) -> int:
+    """The sticky error word of moe_combine (synchronises the device)."""
+    code = ctypes.c_int32(0)
+    _check(lib().moe_comm_error(ctypes.byref(code), int(clear)), "moe_comm_error")
+    return int(code.value)
 
 
 def moe_status_string(st: int) -> str:

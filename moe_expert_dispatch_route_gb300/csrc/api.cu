@@ -90,9 +90,36 @@ cudaError_t ensure_max_dynamic_smem(const void* func, int bytes) {
 
 namespace {
 std::atomic<long long> g_inject_wait_ns{0};
+
+// Sticky error word of the staged dispatch / combine kernels called without a caller
+// flag (moe_dispatch, moe_combine).
+__device__ int32_t g_comm_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_comm_mu;
+struct CommWord {
+    unsigned long long ctx;  // context the address was looked up in
+    int32_t* ptr;
+};
+CommWord g_comm_word[kMaxDevices] = {};
 }  // namespace
 
 int64_t wait_injection_ns() { return g_inject_wait_ns.load(std::memory_order_relaxed); }
+
+// The address of g_comm_error is looked up with the device current, once per context
+// (a device reset followed by a new context gets a fresh lookup).
+int32_t* comm_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    const unsigned long long ctx = current_context_id();
+    std::lock_guard<std::mutex> lk(g_comm_mu);
+    if (!g_comm_word[dev].ptr || ctx == 0 || g_comm_word[dev].ctx != ctx) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_comm_error) != cudaSuccess) return nullptr;
+        g_comm_word[dev] = CommWord{ctx, static_cast<int32_t*>(p)};
+    }
+    return g_comm_word[dev].ptr;
+}
 
 namespace {
 
@@ -142,6 +169,17 @@ moe_status moe_debug_inject_wait(int32_t enable, int64_t timeout_ns) {
     if (enable && timeout_ns <= 0) return MOE_ERR_INVALID_ARG;
     g_inject_wait_ns.store(enable ? (long long)timeout_ns : 0, std::memory_order_relaxed);
     return MOE_OK;
+}
+
+moe_status moe_comm_error(int32_t* code, int32_t clear) {
+    if (!code) return MOE_ERR_INVALID_ARG;
+    int32_t* word = comm_error_word();
+    if (!word) return MOE_ERR_CUDA;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(code, word, sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && clear) e = cudaMemset(word, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return cuda_status(e);
 }
 
 const char* moe_status_string(moe_status s) {

@@ -35,10 +35,43 @@ __device__ __forceinline__ float warp_sum(float v) {
 // amax <= 448 * 2^s (448 = 0.875 * 2^9); amax == 0 gives 0.
 __device__ __forceinline__ int fp8_scale_exp(float amax) {
     if (!(amax > 0.0f)) return 0;
-    int e;
-    float f = frexpf(amax, &e);
-    return (f <= 0.875f) ? e - 9 : e - 8;
+    const uint32_t b = __float_as_uint(amax);
+    const int ef = (int)(b >> 23);  // amax > 0: the sign bit is clear
+    if (ef == 0 || ef == 255) {     // subnormal or infinite: the library's decomposition
+        int e;
+        const float f = frexpf(amax, &e);
+        return (f <= 0.875f) ? e - 9 : e - 8;
+    }
+    // amax = (1 + m / 2^23) * 2^(ef - 127) and 448 = 1.75 * 2^8: s = ef - 135 when the
+    // significand is at most 1.75 (m <= 0.75 * 2^23), else one more
+    return ((b & 0x7fffffu) <= 0x600000u) ? ef - 135 : ef - 134;
 }
+
+// x * 2^n rounded once to nearest even, the value scalbnf(x, n) gives: the product of x
+// and an exact power of two is the correctly rounded value of the same real number.  For
+// n above the normal exponent range, two steps that both scale up (exact unless they
+// overflow, which the one-step result would too); below it, scalbnf itself (two steps
+// down could round twice).
+__device__ __forceinline__ float mul_pow2(float x, int n) {
+    if (n >= -126 && n <= 127) return x * __int_as_float((n + 127) << 23);
+    if (n > 127 && n <= 254) return (x * 0x1p127f) * __int_as_float(n << 23);
+    return scalbnf(x, n);
+}
+
+// 2^-s as two exact factors (m1, m2) for s in [-254, 126]: (x * m1) * m2 equals
+// mul_pow2(x, -s) -- with 2^-s a normal float, m2 = 1 and the one product is the single
+// rounding; above the normal range, m1 = 2^127 and both products scale up exactly.  An
+// FP8 group scale exponent is always in range (at most 119 for a finite amax, at least
+// -157 for a nonzero one).
+struct Pow2Factors {
+    float m1, m2;
+};
+__device__ __forceinline__ Pow2Factors pow2_neg(int s) {
+    const int n = -s;
+    const int n1 = n > 127 ? 127 : n;
+    return {__uint_as_float((uint32_t)(n1 + 127) << 23), __uint_as_float((uint32_t)(n - n1 + 127) << 23)};
+}
+__device__ __forceinline__ float scale_by(float x, const Pow2Factors& f) { return (x * f.m1) * f.m2; }
 
 // Two floats -> two e4m3 codes (round to nearest even, saturating to +-448).
 __device__ __forceinline__ uint16_t f2_to_e4m3x2(float a, float b) {

@@ -397,7 +397,7 @@ moe_status moe_layer_dbo_ex(moe_dbo_handle* h, const moe_config* cfg, const moe_
             }
             case MOE_OP_COMBINE: {
                 char* yu = static_cast<char*>(a->y) + (size_t)t0[u] * H * io_bytes(c.dtype);
-                ce = launch_combine(c, Tu, ye, w_u, slot_of, yu, comm_grid, q);
+                ce = launch_combine(c, Tu, ye, w_u, slot_of, yu, comm_grid, q, nullptr, err);
                 break;
             }
         }
@@ -554,7 +554,7 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
                 ce = launch_ffn(c, fa, ffn_grid, q);
                 break;
             }
-            case MOE_OP_COMBINE: ce = launch_combine(c, Tu, ye, wts, slot_of, xout, comm_grid, q, act); break;
+            case MOE_OP_COMBINE: ce = launch_combine(c, Tu, ye, wts, slot_of, xout, comm_grid, q, act, err); break;
         }
         if (ce != cudaSuccess) {
             if (forked) join_after_failure(h, cs, ms);

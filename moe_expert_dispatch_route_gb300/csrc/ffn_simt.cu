@@ -169,10 +169,11 @@ __global__ void __launch_bounds__(NT) ffn_simt_up_kernel(int NE, int H, int I, c
                 const int s = fp8_scale_exp(amax);
                 if (r < rows_here) {
                     uint8_t* hq = static_cast<uint8_t*>(h) + (row0 + r) * I + n0 + tx * 4;
-                    const uint16_t p0 = f2_to_e4m3x2(scalbnf(hv[0], -s), scalbnf(hv[1], -s));
-                    const uint16_t p1 = f2_to_e4m3x2(scalbnf(hv[2], -s), scalbnf(hv[3], -s));
+                    const Pow2Factors f = pow2_neg(s);
+                    const uint16_t p0 = f2_to_e4m3x2(scale_by(hv[0], f), scale_by(hv[1], f));
+                    const uint16_t p1 = f2_to_e4m3x2(scale_by(hv[2], f), scale_by(hv[3], f));
                     *reinterpret_cast<uint32_t*>(hq) = (uint32_t)p0 | ((uint32_t)p1 << 16);
-                    if (tx == 0) h_scale[(row0 + r) * (I / kQG) + nt] = scalbnf(1.0f, s);
+                    if (tx == 0) h_scale[(row0 + r) * (I / kQG) + nt] = mul_pow2(1.0f, s);
                 }
             } else if (r < rows_here) {
 #pragma unroll

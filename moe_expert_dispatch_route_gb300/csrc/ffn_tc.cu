@@ -910,20 +910,21 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
             amax = fmaxf(amax, s.xval[(par * 2 + 1 - half) * 128 + r]);
             if (valid) {
                 const int se = fp8_scale_exp(amax);
+                const Pow2Factors f = pow2_neg(se);
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const uint32_t* src = i < 8 ? g0 + 4 * i : g1 + 4 * (i - 8);
-                    const uint16_t lo = f2_to_e4m3x2(scalbnf(__uint_as_float(src[0]), -se),
-                                                     scalbnf(__uint_as_float(src[1]), -se));
-                    const uint16_t hi = f2_to_e4m3x2(scalbnf(__uint_as_float(src[2]), -se),
-                                                     scalbnf(__uint_as_float(src[3]), -se));
+                    const uint16_t lo = f2_to_e4m3x2(scale_by(__uint_as_float(src[0]), f),
+                                                     scale_by(__uint_as_float(src[1]), f));
+                    const uint16_t hi = f2_to_e4m3x2(scale_by(__uint_as_float(src[2]), f),
+                                                     scale_by(__uint_as_float(src[3]), f));
                     w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + row * p.I + t.nt * 128 + 64 * half);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                if (half == 0) p.out_scale[(int64_t)t.nt * p.max_rows + row] = scalbnf(1.0f, se);
+                if (half == 0) p.out_scale[(int64_t)t.nt * p.max_rows + row] = mul_pow2(1.0f, se);
             }
         } else if (kComb) {
             // fused combine: the accumulator in two passes of 64 columns (registers for the

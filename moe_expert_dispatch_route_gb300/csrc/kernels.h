@@ -29,6 +29,10 @@ unsigned long long current_context_id();
 // now on first wait this long on a barrier nothing arrives on, then report
 // MOE_ERR_TIMEOUT and skip its work; 0 = off (the default).
 int64_t wait_injection_ns();
+// Device address, in the context current on this thread, of the library's sticky error
+// word: the staged combine kernel called on its own (no caller flag) stores
+// MOE_ERR_TIMEOUT there when a bounded wait runs out.  NULL if it cannot be looked up.
+int32_t* comm_error_word();
 // Raises the dynamic shared memory limit of a kernel to `bytes`, once per context
 // (thread-safe); later calls in the same context return at once.
 cudaError_t ensure_max_dynamic_smem(const void* func, int bytes);
@@ -72,9 +76,11 @@ cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int
 // fused gather, fp8: x [T][H] bf16 -> x_q [T][H] e4m3 + scales column-major [H/128][scale_cs]
 cudaError_t launch_quantize_rows(const moe_config& c, int T, const void* x, void* xq, float* xs, int64_t scale_cs,
                                  int grid_cap, cudaStream_t st);
+// err: device int32 receiving MOE_ERR_TIMEOUT if a bounded wait of the staged kernels
+// runs out (NULL: the library's own sticky word, read by moe_comm_error).
 cudaError_t launch_combine(const moe_config& c, int T, const void* ye, const float* w,
                            const int32_t* slot_of, void* y, int grid_cap, cudaStream_t st,
-                           const void* resid = nullptr);
+                           const void* resid = nullptr, int32_t* err = nullptr);
 
 // FFN: scratch = h [max_rows][I] (+ fp8 scales) followed by the kernels' own scratch.
 size_t ffn_scratch_bytes(const moe_config& c, int64_t max_rows);

@@ -78,6 +78,59 @@ __device__ __forceinline__ void wait_on_nothing(uint64_t* never, uint64_t ns) {
     }
 }
 
+// Bounded wait without an abort flag: gives up (returns false) after kWaitTimeoutNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0 && globaltimer() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
+// ---------------------------------------------------------------- bulk (untiled) async copies
+// Both addresses 16-byte aligned, `bytes` a multiple of 16.  A load signals `bar` with
+// `bytes` transaction bytes when its data has landed in shared memory.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(static_cast<uint64_t>(__cvta_generic_to_global(src))), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+// Shared -> global; completes as part of this thread's current bulk async-group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     static_cast<uint64_t>(__cvta_generic_to_global(dst))),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until at most N of this thread's committed bulk groups are incomplete (writes done).
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- small async copies (cp.async)
+// 4 bytes global -> shared, tracked by this thread's cp.async groups: no register waits
+// on the data, so a warp can keep many small loads in flight.
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+                 "l"(static_cast<uint64_t>(__cvta_generic_to_global(src)))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Lets the next kernel on the stream start its prologue before this one finishes.
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -30,7 +30,7 @@ def _worker(rank, world, port, out):
     assert (r, w, lr) == (rank, world, rank)
     t = bench.max_over_ranks(1.0 + rank, world)
     bench.barrier(world)
-    args = type("A", (), dict(workload="tiny", T=8, routing=None, capacity=None, steps=1, warmup=0))()
+    args = type("A", (), dict(workload="tiny", T=8, experts=None, routing=None, capacity=None, steps=1, warmup=0))()
     ref, _ = bench.run_reference(args, rank, world, rank) if rank != 0 else (None, None)
     out[rank] = (t, ref is None)
     dist.destroy_process_group()
