@@ -47,7 +47,18 @@ from moe_expert_dispatch_route_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (route->dispatch->GEMM->combine, DBO) at 1 GB300; % roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-COMM_SMS = 16
+# SMs given to the comm-side steps while they overlap an FFN.  Measured on GB300 (0, 8,
+# 16, 24, 32 SMs): decode-sized ubatches gain from 16, where the FFN streams weights and
+# the comm kernels are latency-bound; prefill ubatches are fastest with no split at all,
+# because there the FFN is held by a GPU-wide limit and kernels beside it only take
+# bandwidth from it (DeepSeek-V3 T=16384: 8.41 ms with no split, 8.73 with 16 SMs).
+COMM_SMS_DECODE = 16
+DECODE_UBATCH_MAX = 512
+
+
+def default_comm_sms(wl) -> int:
+    ub = wl.split if (wl.T >= 4 and 0 < wl.split < wl.T) else wl.T
+    return COMM_SMS_DECODE if ub <= DECODE_UBATCH_MAX else 0
 DEFAULT_WORKLOAD = ("dsv3", 16384)
 
 
@@ -66,7 +77,9 @@ def parse():
     ap.add_argument("--routing", default=None, choices=[None, "uniform", "zipf"])
     ap.add_argument("--capacity", type=int, default=None,
                     help="rows per expert per ubatch (worst-token layout); -1 = the ubatch size")
-    ap.add_argument("--comm-sms", type=int, default=COMM_SMS)
+    ap.add_argument("--comm-sms", type=int, default=None,
+                    help="SM budget of the comm-side steps beside an FFN (default: 16 for ubatches of at "
+                         "most 512 tokens, else 0 = no split)")
     ap.add_argument("--fused", default="none", choices=["none", "gather", "combine", "both"],
                     help="time the layer with the gather fused into the expert GEMM and / or the combine into "
                          "its epilogue; every other mode is timed beside it")
@@ -293,7 +306,7 @@ def run_ours(args, rank, world, local):
     comm = torch.cuda.Stream(device=dev)
     compute = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()  # inputs and zeroed buffers were made on the current stream
-    comm_sms = args.comm_sms
+    comm_sms = args.comm_sms if args.comm_sms is not None else default_comm_sms(wl)
 
     modes = {"none": 0, "gather": B.LAYER_FUSED_GATHER, "combine": B.LAYER_FUSED_COMBINE, "both": B.LAYER_FUSED}
     flags = modes[args.fused]
@@ -431,6 +444,7 @@ def run_stack(args, rank, world, local):
 
     wl = workload(args)
     L = args.stack
+    comm_sms = args.comm_sms if args.comm_sms is not None else default_comm_sms(wl)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = B.config_of(wl)
@@ -457,10 +471,10 @@ def run_stack(args, rank, world, local):
     def graph(split, before):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(compute):
-            B.moe_stack_dbo(h, cfg, sa, T, split, 4, wl.capacity, wl.align, args.comm_sms, before, compute, comm)
+            B.moe_stack_dbo(h, cfg, sa, T, split, 4, wl.capacity, wl.align, comm_sms, before, compute, comm)
             torch.cuda.synchronize()
             with torch.cuda.graph(g, stream=compute):
-                B.moe_stack_dbo(h, cfg, sa, T, split, 4, wl.capacity, wl.align, args.comm_sms, before, compute, comm)
+                B.moe_stack_dbo(h, cfg, sa, T, split, 4, wl.capacity, wl.align, comm_sms, before, compute, comm)
         torch.cuda.synchronize()
         return g
 
@@ -492,7 +506,7 @@ def run_stack(args, rank, world, local):
            "value": round(T * world / (ms_fix / 1e3), 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_fix, 5), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "fp8e4m3"}[wl.dtype],
-           "data": "synthetic", "config": {"workload": wl.describe(), "layers": L, "comm_sms": args.comm_sms},
+           "data": "synthetic", "config": {"workload": wl.describe(), "layers": L, "comm_sms": comm_sms},
            "clocks": clocks,
            "stack": {"ms_event_before_yield": round(ms_fix, 5), "ms_event_after_yield": round(ms_old, 5),
                      "gain_of_event_before_yield": round(ms_old / ms_fix, 4),

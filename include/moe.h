@@ -299,10 +299,13 @@ MOE_API size_t moe_layer_workspace_size(const moe_config* cfg, int32_t T, int32_
  *           T < min_tokens also runs unsplit (never an empty ubatch, [B] commit list).
  * capacity  0 = exact layout; > 0 = worst-token layout with that many rows per expert
  *           per ubatch (must be >= the ubatch's token count for no overflow).
- * comm_sms  CTAs given to route/plan/dispatch/combine; the expert FFN gets the
- *           remaining SMs.  0 = no split of the GPU.
+ * comm_sms  SMs given to route/plan/dispatch/combine while they overlap an expert FFN
+ *           (each of their kernels is capped at as many CTAs as fit on that many SMs);
+ *           the FFN gets one CTA on each remaining SM.  Steps that overlap nothing get
+ *           the whole GPU.  0 = no split of the GPU.
  * compute, comm  the two streams; comm == compute runs the identical two-ubatch
- *           schedule serialised on one stream.
+ *           schedule serialised on one stream, every kernel on the whole GPU (the SM
+ *           budget applies only when the streams differ).
  * The call resets *err_flag to 0 on the compute stream before its kernels run. */
 MOE_API moe_status moe_layer_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_layer_args* args,
                          int32_t T, int32_t split, int32_t min_tokens, int32_t capacity,

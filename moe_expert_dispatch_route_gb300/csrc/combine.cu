@@ -308,6 +308,8 @@ constexpr int kStageSmemBudget = 233472 / kStageCtasPerSm - 2048;
 constexpr int kStageChunkCap = 4096;
 
 
+int combine_ctas_per_sm() { return kStageCtasPerSm; }
+
 cudaError_t launch_combine(const moe_config& c, int T, const void* ye, const float* w,
                            const int32_t* slot_of, void* y, int grid_cap, cudaStream_t st, const void* resid,
                            int32_t* err) {

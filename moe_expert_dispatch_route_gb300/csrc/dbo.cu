@@ -288,8 +288,15 @@ moe_status moe_layer_dbo_ex(moe_dbo_handle* h, const moe_config* cfg, const moe_
     const int tn[2] = {s, T - s};
 
     const int sms = device_info().num_sms;
-    const int comm_cap = comm_sms > 0 ? comm_sms : sms * 8;
-    const int ffn_cap = comm_sms > 0 ? (sms - comm_sms > 1 ? sms - comm_sms : 1) : sms * 8;
+    // comm_sms is an SM budget: a comm-side kernel beside an FFN gets as many CTAs as fit
+    // on that many SMs (kCommCtasPerSm for the 256-thread kernels, the staged combine's
+    // own count), the FFN one CTA on each remaining SM
+    // (only when the two streams differ: serialised on one stream nothing runs beside an
+    // FFN, and every kernel gets the whole GPU)
+    const bool budget = comm_sms > 0 && cs != ms;
+    const int comm_cap = budget ? comm_sms * kCommCtasPerSm : sms * 8;
+    const int comb_cap = budget ? comm_sms * combine_ctas_per_sm() : sms * 8;
+    const int ffn_cap = budget ? (sms - comm_sms > 1 ? sms - comm_sms : 1) : sms * 8;
 
     char* ws = static_cast<char*>(a->workspace);
     int32_t* err = a->err_flag ? a->err_flag : reinterpret_cast<int32_t*>(ws);
@@ -324,7 +331,7 @@ moe_status moe_layer_dbo_ex(moe_dbo_handle* h, const moe_config* cfg, const moe_
         // route / plan / dispatch, ubatch 0's combine); ubatch 0's first steps and
         // ubatch 1's combine run alone and get the whole GPU
         const bool overlapped = (u == 1 && op.op != MOE_OP_COMBINE) || (u == 0 && op.op == MOE_OP_COMBINE);
-        const int comm_grid = (two && overlapped) ? comm_cap : sms * 8;
+        const int comm_grid = (two && overlapped) ? (op.op == MOE_OP_COMBINE ? comb_cap : comm_cap) : sms * 8;
         const int ffn_grid = two ? ffn_cap : sms * 8;
         // the clustered head (clusters of up to 8 CTAs) only where nothing else runs: beside
         // an FFN the free SMs are scattered over the GPCs and a cluster might not fit
@@ -491,8 +498,10 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
     const int t0[2] = {0, s};
     const int tn[2] = {s, T - s};
     const int sms = device_info().num_sms;
-    const int comm_cap = comm_sms > 0 ? comm_sms : sms * 8;
-    const int ffn_cap = comm_sms > 0 ? (sms - comm_sms > 1 ? sms - comm_sms : 1) : sms * 8;
+    const bool budget = comm_sms > 0 && cs != ms;  // as in moe_layer_dbo_ex
+    const int comm_cap = budget ? comm_sms * kCommCtasPerSm : sms * 8;
+    const int comb_cap = budget ? comm_sms * combine_ctas_per_sm() : sms * 8;
+    const int ffn_cap = budget ? (sms - comm_sms > 1 ? sms - comm_sms : 1) : sms * 8;
     char* ws = static_cast<char*>(a->workspace);
     int32_t* err = a->err_flag ? a->err_flag : reinterpret_cast<int32_t*>(ws);
     const UbLayout& U = S.ub;
@@ -525,7 +534,7 @@ moe_status moe_stack_dbo(moe_dbo_handle* h, const moe_config* cfg, const moe_sta
         // plan and dispatch (beside F0) and ubatch 0's combine (beside F1).  Ubatch 0's
         // head and ubatch 1's combine run beside a stand-in block only and take the GPU.
         const bool beside_ffn = two && (op.op == MOE_OP_COMBINE ? u == 0 : u == 1);
-        const int comm_grid = beside_ffn ? comm_cap : sms * 8;
+        const int comm_grid = beside_ffn ? (op.op == MOE_OP_COMBINE ? comb_cap : comm_cap) : sms * 8;
         const int ffn_grid = two ? ffn_cap : sms * 8;
         cudaError_t ce = cudaSuccess;
         switch (op.op) {

@@ -76,6 +76,11 @@ cudaError_t launch_dispatch(const moe_config& c, int T, const void* x, const int
 // fused gather, fp8: x [T][H] bf16 -> x_q [T][H] e4m3 + scales column-major [H/128][scale_cs]
 cudaError_t launch_quantize_rows(const moe_config& c, int T, const void* x, void* xq, float* xs, int64_t scale_cs,
                                  int grid_cap, cudaStream_t st);
+// Resident CTAs per SM of the 256-thread comm-side kernels (route, plan, dispatch,
+// quantize_rows: 2048 threads per SM, registers well under the limit) and of the staged
+// combine: an SM budget for them is that many CTAs per SM.
+constexpr int kCommCtasPerSm = 8;
+int combine_ctas_per_sm();
 // err: device int32 receiving MOE_ERR_TIMEOUT if a bounded wait of the staged kernels
 // runs out (NULL: the library's own sticky word, read by moe_comm_error).
 cudaError_t launch_combine(const moe_config& c, int T, const void* ye, const float* w,

@@ -20,7 +20,7 @@ from helpers import check_close, np_f32, np_weights, ocfg
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-COMM_SMS = 16  # the benchmark's SM budget for the comm-side kernels
+COMM_SMS = 16  # an SM budget for the comm-side kernels (the benchmark's at decode-sized ubatches)
 
 
 class Layer:

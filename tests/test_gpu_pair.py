@@ -6,8 +6,8 @@ oracle, through the C ABI.
   the pair idle), a shared expert whose last pair tile is ragged in the peer's half,
   one-k-block tiles, several tiles per pair, capacity layout; every output element
   against the oracle.  The same shapes with MOE_FFN_TILE=single must agree too.
-* At full size, in the benchmark's launch configuration (16 SMs left to the comm
-  kernels) and the kernels the library picks: every row of the busiest Zipf-routed
+* At full size, in the benchmark's launch configuration (prefill ubatches: the FFN on
+  every SM, no split of the GPU) and the kernels the library picks: every row of the busiest Zipf-routed
   expert of the Qwen3-30B-A3B prefill layer (fp8) and of the DeepSeek-V2-Lite layer at
   T=4096 (bf16: CTA-pair tiles), and for the DeepSeek-V3 prefill layer rows from every
   256-row block (both halves, the block edges) of the busiest routed expert and of the
@@ -31,7 +31,7 @@ from helpers import check_close, np_f32
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-COMM_SMS = 16
+COMM_SMS = 0  # the benchmark's SM budget at prefill-sized ubatches: no split
 
 FORCED_SCRIPT = r"""
 import sys, numpy as np, torch
@@ -72,7 +72,8 @@ def test_forced_tile_family_matches_oracle(tile):
 
 def _ubatch0_ffn(wl):
     """Route, plan, dispatch and the expert FFN of the first ubatch through the C ABI, in
-    the layer's launch configuration (fp8: column-major activation scales; SM budget)."""
+    the layer's launch configuration (fp8: column-major activation scales; the FFN on
+    sms - COMM_SMS CTAs)."""
     cfg = B.config_of(wl)
     fp8 = wl.dtype == "fp8"
     T0 = wl.split
