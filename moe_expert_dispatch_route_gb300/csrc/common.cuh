@@ -73,6 +73,12 @@ __device__ __forceinline__ Pow2Factors pow2_neg(int s) {
 }
 __device__ __forceinline__ float scale_by(float x, const Pow2Factors& f) { return (x * f.m1) * f.m2; }
 
+// SwiGLU of the tensor-core FFNs: silu(g) * u = g / (1 + e^-g) * u with the fast
+// exponential and division intrinsics (a few ulp of relative error, far below the bf16 /
+// e4m3 rounding of h that follows).  The limits stay exact: for very negative g the
+// divisor overflows to infinity and the quotient is 0; for very positive g it is g.
+__device__ __forceinline__ float silu_mul_fast(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
 // Two floats -> two e4m3 codes (round to nearest even, saturating to +-448).
 __device__ __forceinline__ uint16_t f2_to_e4m3x2(float a, float b) {
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);

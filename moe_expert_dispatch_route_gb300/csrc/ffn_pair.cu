@@ -451,7 +451,7 @@ __device__ __forceinline__ void release_acc(const Smem& s, int buf, uint32_t ran
     }
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
 
 // Eight warps, two per TMEM lane quarter; `half` selects half of the tile's columns
 // (up: 64 gate + the matching 64 up columns; down: 128 of the 256).
@@ -493,8 +493,8 @@ __device__ void epilogue(const PairParams& p, const Smem& s, int total, uint32_t
             if (busy) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float ha = silu_mul(__uint_as_float(g0[i]), __uint_as_float(u0[i]));
-                    const float hb = silu_mul(__uint_as_float(g1[i]), __uint_as_float(u1[i]));
+                    const float ha = silu_mul_fast(__uint_as_float(g0[i]), __uint_as_float(u0[i]));
+                    const float hb = silu_mul_fast(__uint_as_float(g1[i]), __uint_as_float(u1[i]));
                     g0[i] = __float_as_uint(ha);
                     g1[i] = __float_as_uint(hb);
                     amax = fmaxf(amax, fmaxf(fabsf(ha), fabsf(hb)));

@@ -470,7 +470,7 @@ __device__ void mma_issuer(const TcParams& p, const Smem& s, int total, uint32_t
     }
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
 
 template <bool kUp, bool kComb>
 __device__ void epilogue(const TcParams& p, const Smem& s, int total, uint32_t tmem_base) {
@@ -502,8 +502,8 @@ __device__ void epilogue(const TcParams& p, const Smem& s, int total, uint32_t t
                     uint32_t* w = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        w[i] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                                           silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+                        w[i] = pack_bf16x2(silu_mul_fast(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                           silu_mul_fast(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
                     uint4* dst = reinterpret_cast<uint4*>(hrow + c);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = v[i];
@@ -885,8 +885,8 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float ga = __uint_as_float(g0[i]), gb = __uint_as_float(g1[i]);
-                    const float ha = ga / (1.0f + expf(-ga)) * __uint_as_float(u0[i]);
-                    const float hb = gb / (1.0f + expf(-gb)) * __uint_as_float(u1[i]);
+                    const float ha = silu_mul_fast(ga, __uint_as_float(u0[i]));
+                    const float hb = silu_mul_fast(gb, __uint_as_float(u1[i]));
                     g0[i] = __float_as_uint(ha);
                     g1[i] = __float_as_uint(hb);
                     amax = fmaxf(amax, fmaxf(fabsf(ha), fabsf(hb)));
