@@ -61,8 +61,9 @@ constexpr int kSfCol = 256;
 constexpr int kSfStageBytes = 1536;  // A scales, B scales of rows 0-127, of rows 128-255 (512 B each)
 constexpr int kMaxStages = 6;
 constexpr int kNumBars = 2 * kMaxStages + 2 + 2 + 2;  // full, empty, tmem full, tmem empty, drain, never
-constexpr size_t kSmemTail =
-    kNumBars * 8 + 16 + 3 * (kMaxExperts + 1) * sizeof(int) + 512 * sizeof(float) + 256 * sizeof(int);
+constexpr int kOutSlotBytes = 2048;  // per epilogue warp: 32 rows x 64 bytes of output staging
+constexpr size_t kSmemTail = kNumBars * 8 + 16 + 3 * (kMaxExperts + 1) * sizeof(int) + 512 * sizeof(float) +
+                             256 * sizeof(int) + 128 + 8 * kOutSlotBytes;
 constexpr size_t smem_bytes(int stages, int stage_bytes, int sf_bytes) {
     return 1024 + (size_t)stages * (stage_bytes + sf_bytes) + kSmemTail;
 }
@@ -137,6 +138,7 @@ struct Smem {
     int* off;
     float* xval;         // fp8 up epilogue: [2 parities][2 halves][128 rows] partial amax
     volatile int* xseq;  // [2 halves][128 rows] tile sequence number of the value
+    uint4* oslot;        // epilogue output staging: kOutSlotBytes per epilogue warp
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw, int stages, int stage_bytes, int sf_bytes) {
@@ -159,7 +161,30 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int stages, int stage_bytes,
     s.off = s.cnt + (kMaxExperts + 1);
     s.xval = reinterpret_cast<float*>(s.off + (kMaxExperts + 1));
     s.xseq = reinterpret_cast<volatile int*>(s.xval + 512);
+    s.oslot = reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(s.xseq + 256) + 127) & ~uintptr_t(127));
     return s;
+}
+
+// Stores 64 bytes of each of a warp's 32 rows (lane i holds row i's words w[0..15],
+// registers: every index is a constant after unrolling)
+// through the warp's shared slot: written with the 16-byte chunks XOR-swizzled by row
+// (no bank conflicts either way), read back so that lane l holds chunk l % 4 of row
+// l / 4 + 8j, then stored 8 rows x 64 contiguous bytes per instruction instead of 32
+// rows x 16 bytes.  base: the warp's first row's destination; pitch: bytes between
+// rows; nrows: rows of the 32 to write.  Whole warp; 16-byte aligned base and pitch.
+__device__ __forceinline__ void store_rows64(uint4* slot, const uint32_t* w, uint8_t* base, int64_t pitch,
+                                             int nrows, int lane) {
+    const int f = (lane >> 1) & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) slot[lane * 4 + (i ^ f)] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int rr = (lane >> 2) + 8 * j;
+        const uint4 v = slot[rr * 4 + ((lane & 3) ^ ((rr >> 1) & 3))];
+        if (rr < nrows) reinterpret_cast<uint4*>(base + rr * pitch)[lane & 3] = v;
+    }
+    __syncwarp();
 }
 
 __device__ __forceinline__ void fail(const Smem& s, int32_t* err) {
@@ -489,36 +514,38 @@ __device__ void epilogue(const TcParams& p, const Smem& s, int total, uint32_t t
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN);
         const bool valid = r < t.rows;
         const int64_t row = (int64_t)t.row0 + r;
+        // this warp's 32 rows: those of the tile, for the staged stores
+        const int nrows = min(32, max(0, t.rows - q * 32));
+        uint4* slot = s.oslot + (size_t)(warp - 2) * (kOutSlotBytes / 16);
         if (kUp) {
-            uint16_t* hrow = static_cast<uint16_t*>(p.out) + row * p.I + t.nt * 128;
+            uint8_t* hbase = reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(p.out) +
+                                                        ((int64_t)t.row0 + q * 32) * p.I + t.nt * 128);
 #pragma unroll 1
             for (int c = 0; c < 128; c += 32) {
                 uint32_t g[32], u[32];
                 tc::tmem_ld32(tb + c, g);
                 tc::tmem_ld32(tb + 128 + c, u);
                 tc::tmem_wait_ld();
-                if (valid) {
-                    uint4 v[4];
-                    uint32_t* w = reinterpret_cast<uint32_t*>(v);
+                if (nrows > 0) {
+                    uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         w[i] = pack_bf16x2(silu_mul_fast(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
                                            silu_mul_fast(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
-                    uint4* dst = reinterpret_cast<uint4*>(hrow + c);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = v[i];
+                    store_rows64(slot, w, hbase + c * 2, (int64_t)p.I * 2, nrows, lane);
                 }
             }
         } else {
-            uint16_t* yrow = static_cast<uint16_t*>(p.out) + row * p.H + t.nt * kBN;
+            uint8_t* ybase = reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(p.out) +
+                                                        ((int64_t)t.row0 + q * 32) * p.H + t.nt * kBN);
             const uint16_t* rrow = p.resid ? static_cast<const uint16_t*>(p.resid) + row * p.H + t.nt * kBN : nullptr;
 #pragma unroll 1
             for (int c = 0; c < kBN; c += 32) {
                 uint32_t a[32];
                 tc::tmem_ld32(tb + c, a);
                 tc::tmem_wait_ld();
-                if (valid) {
-                    if (rrow) {  // residual: out = resid + product, one rounding
+                if (valid && rrow) {  // residual: out = resid + product, one rounding
+                    {
                         const uint4* rr = reinterpret_cast<const uint4*>(rrow + c);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -533,13 +560,18 @@ __device__ void epilogue(const TcParams& p, const Smem& s, int total, uint32_t t
                             }
                         }
                     }
-                    uint4 v[4];
-                    uint32_t* w = reinterpret_cast<uint32_t*>(v);
+                }
+                uint32_t w[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-                    uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+                for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                if (kComb) {  // each lane its own row: the fused combine fences and counts that row
+                    if (valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(ybase + (int64_t)lane * p.H * 2 + c * 2);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = v[i];
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
+                } else if (nrows > 0) {
+                    store_rows64(slot, w, ybase + c * 2, (int64_t)p.H * 2, nrows, lane);
                 }
             }
         }
@@ -905,10 +937,11 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
                     break;
                 }
             }
+            ok = __all_sync(0xffffffffu, ok);  // a wait that ran out ends the tile for the whole warp
             if (!ok) break;
             __threadfence_block();
             amax = fmaxf(amax, s.xval[(par * 2 + 1 - half) * 128 + r]);
-            if (valid) {
+            if (busy) {
                 const int se = fp8_scale_exp(amax);
                 const Pow2Factors f = pow2_neg(se);
                 uint32_t w[16];
@@ -921,10 +954,11 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
                                                      scale_by(__uint_as_float(src[3]), f));
                     w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + row * p.I + t.nt * 128 + 64 * half);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                if (half == 0) p.out_scale[(int64_t)t.nt * p.max_rows + row] = mul_pow2(1.0f, se);
+                // this warp's 32 rows x 64 bytes of h, staged for row-contiguous stores
+                uint8_t* hbase = static_cast<uint8_t*>(p.out) + ((int64_t)t.row0 + q * 32) * p.I + t.nt * 128 + 64 * half;
+                store_rows64(s.oslot + (size_t)(warp - kF8FirstEpiWarp) * (kOutSlotBytes / 16), w, hbase, p.I,
+                             min(32, t.rows - q * 32), lane);
+                if (valid && half == 0) p.out_scale[(int64_t)t.nt * p.max_rows + row] = mul_pow2(1.0f, se);
             }
         } else if (kComb) {
             // fused combine: the accumulator in two passes of 64 columns (registers for the
@@ -961,18 +995,18 @@ __device__ void epilogue_f8(const TcParams& p, const Smem& s, int total, uint32_
                 tc::tmem_wait_ld();
             }
             release_acc(s, buf);
-            if (valid) {
-                uint4* dst =
-                    reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.H + t.nt * G::N + 128 * half);
+            if (busy) {  // this warp's 32 rows, 32 columns (64 bytes) a pass, staged stores
+                uint8_t* ybase = reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(p.out) +
+                                                            ((int64_t)t.row0 + q * 32) * p.H + t.nt * G::N + 128 * half);
+                uint4* slot = s.oslot + (size_t)(warp - kF8FirstEpiWarp) * (kOutSlotBytes / 16);
+                const int nrows = min(32, t.rows - q * 32);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[4 * c + i] =
-                            make_uint4(pack_bf16x2(__uint_as_float(a[c][8 * i]), __uint_as_float(a[c][8 * i + 1])),
-                                       pack_bf16x2(__uint_as_float(a[c][8 * i + 2]), __uint_as_float(a[c][8 * i + 3])),
-                                       pack_bf16x2(__uint_as_float(a[c][8 * i + 4]), __uint_as_float(a[c][8 * i + 5])),
-                                       pack_bf16x2(__uint_as_float(a[c][8 * i + 6]), __uint_as_float(a[c][8 * i + 7])));
+                    for (int i = 0; i < 16; ++i)  // packed in place: word i from words 2i, 2i+1
+                        a[c][i] = pack_bf16x2(__uint_as_float(a[c][2 * i]), __uint_as_float(a[c][2 * i + 1]));
+                    store_rows64(slot, a[c], ybase + 64 * c, (int64_t)p.H * 2, nrows, lane);
+                }
             }
         }
         if (++buf == G::AccBufs) {
