@@ -68,9 +68,13 @@ struct Cfg {
 };
 
 constexpr size_t kTail = 64 * 8 + 16 + 3 * (kMaxExperts + 1) * sizeof(int) + 512 * sizeof(float) + 256 * sizeof(int);
+// bf16: per epilogue warp, 32 rows x 64 bytes of output staging (the fp8 kernels have no
+// room left for it and store row by row)
+constexpr int kOutSlotBytes = 2048;
 template <bool kFp8>
 constexpr size_t smem_bytes() {
-    return 1024 + (size_t)kStages * (kStageBytes + Cfg<kFp8>::SfBytes) + kTail;
+    return 1024 + (size_t)kStages * (kStageBytes + Cfg<kFp8>::SfBytes) + kTail +
+           (kFp8 ? 0 : 128 + (size_t)kEpiWarps * kOutSlotBytes);
 }
 
 struct PairParams {
@@ -109,6 +113,7 @@ struct Smem {
     int* off;
     float* xval;
     volatile int* xseq;
+    uint4* oslot;  // bf16: kOutSlotBytes per epilogue warp
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw, int sf_bytes) {
@@ -131,7 +136,26 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int sf_bytes) {
     s.off = s.cnt + (kMaxExperts + 1);
     s.xval = reinterpret_cast<float*>(s.off + (kMaxExperts + 1));
     s.xseq = reinterpret_cast<volatile int*>(s.xval + 512);
+    s.oslot = reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(s.xseq + 256) + 127) & ~uintptr_t(127));
     return s;
+}
+
+// Stores 64 bytes of each of a warp's 32 rows (lane i holds row i's words w[0..15])
+// through the warp's shared slot, 16-byte chunks XOR-swizzled by row, so that each
+// global store instruction covers 8 rows x 64 contiguous bytes.  Whole warp.
+__device__ __forceinline__ void store_rows64(uint4* slot, const uint32_t* w, uint8_t* base, int64_t pitch, int nrows,
+                                             int lane) {
+    const int f = (lane >> 1) & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) slot[lane * 4 + (i ^ f)] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int rr = (lane >> 2) + 8 * j;
+        const uint4 v = slot[rr * 4 + ((lane & 3) ^ ((rr >> 1) & 3))];
+        if (rr < nrows) reinterpret_cast<uint4*>(base + rr * pitch)[lane & 3] = v;
+    }
+    __syncwarp();
 }
 
 __device__ __forceinline__ void fail(const Smem& s, int32_t* err) {
@@ -536,16 +560,19 @@ __device__ void epilogue(const PairParams& p, const Smem& s, int total, uint32_t
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                     if (half == 0) p.out_scale[(int64_t)t.nt * p.max_rows + row] = mul_pow2(1.0f, se);
                 }
-            } else if (valid) {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.I + t.nt * 128 + 64 * half);
+            } else if (busy) {  // this warp's 32 rows x 64 columns of h, staged stores
+                uint8_t* hbase = reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(p.out) +
+                                                            ((int64_t)t.row0 + (int)rank * kRows + q * 32) * p.I +
+                                                            t.nt * 128 + 64 * half);
+                uint4* slot = s.oslot + (size_t)(warp - kFirstEpiWarp) * (kOutSlotBytes / 16);
+                const int nrows = min(32, my_rows - q * 32);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t* src = i < 4 ? g0 + 8 * i : g1 + 8 * (i - 4);
-                    dst[i] = make_uint4(pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1])),
-                                        pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3])),
-                                        pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5])),
-                                        pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7])));
+                for (int i = 0; i < 16; ++i) {  // packed in place
+                    g0[i] = pack_bf16x2(__uint_as_float(g0[2 * i]), __uint_as_float(g0[2 * i + 1]));
+                    g1[i] = pack_bf16x2(__uint_as_float(g1[2 * i]), __uint_as_float(g1[2 * i + 1]));
                 }
+                store_rows64(slot, g0, hbase, (int64_t)p.I * 2, nrows, lane);
+                store_rows64(slot, g1, hbase + 64, (int64_t)p.I * 2, nrows, lane);
             }
         } else {
             uint32_t a[4][32];  // columns 128*half .. +127
@@ -555,7 +582,20 @@ __device__ void epilogue(const PairParams& p, const Smem& s, int total, uint32_t
                 tc::tmem_wait_ld();
             }
             release_acc(s, buf, rank, leader_tempty);
-            if (valid) {
+            if (!kFp8 && busy) {  // this warp's 32 rows x 128 columns, staged stores
+                uint8_t* ybase = reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(p.out) +
+                                                            ((int64_t)t.row0 + (int)rank * kRows + q * 32) * p.H +
+                                                            t.nt * kN + 128 * half);
+                uint4* slot = s.oslot + (size_t)(warp - kFirstEpiWarp) * (kOutSlotBytes / 16);
+                const int nrows = min(32, my_rows - q * 32);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)  // packed in place
+                        a[c][i] = pack_bf16x2(__uint_as_float(a[c][2 * i]), __uint_as_float(a[c][2 * i + 1]));
+                    store_rows64(slot, a[c], ybase + 64 * c, (int64_t)p.H * 2, nrows, lane);
+                }
+            } else if (valid) {
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.H + t.nt * kN + 128 * half);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
